@@ -1,0 +1,370 @@
+#!/usr/bin/env python3
+"""Benchmark: packed varlen non-causal attention TFLOP/s on the Ref2VA-shaped
+packed sequence (S = 20,423 tokens in one joint document, 21 heads x 128).
+
+One step = the whole per-block hot path on device-resident inputs: the q/k
+prologue (RMSNorm + rot96 RoPE) and the packed varlen forward.  The plan
+(cu_seqlens, grid, rope table, work list) is built once per request and is
+step-invariant, so it is built before the timed region and timed separately.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the fp64 CPU oracle on bounded samples of the same
+workload (the reference arm).  Multi-GPU (under torchrun): every rank runs an
+independent replica of the workload; no data-path collective exists.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+WORKLOAD = 3  # the S = 20,423 Ref2VA-shaped packed sequence
+METRIC = "packed varlen non-causal attention TFLOP/s and % of GB300 bf16 peak"
+UNIT = "TFLOP/s"
+FWD_SOURCE = os.path.join(ROOT, "packed_varlen_non_gb300", "csrc", "attn_fwd_mma.cu")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_fwd_ref2va_traffic.json")
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return {"bf16_tflops": float(p["bf16_tflops"]), "hbm_gbs": float(p["hbm_gbs"]),
+                "source": "measured"}
+    return {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def workload_config(w, extra=None):
+    cfg = {"workload": w.name, "S": w.S, "heads": w.num_heads, "head_dim": w.head_dim,
+           "docs": len(w.docs), "doc_lengths": w.doc_lengths[:16],
+           "flops_per_step": w.flops(),
+           "step": "qk_prologue (RMSNorm + rot96 RoPE on q and k) + packed varlen forward",
+           "l2": "inputs larger than L2: q, k, v, q_hat, k_hat, o are 6 x 110 MB vs 129 MB L2",
+           "inputs": "splitmix64-seeded bf16 N(0,1); k x per-channel LogNormal(0,0.5); gains N(1,0.1)"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+# ------------------------------------------------------------ oracle leg ----
+
+def oracle_sample(w, t, budget_s: float, heads=None, chunk=512):
+    """Runs the fp64 oracle (prologue + two-pass attention) on query-row chunks
+    until the time budget is used; returns (flops, seconds, rows, heads)."""
+    from oracle import attention as oatt
+    from oracle import plan as oplan
+    from oracle import prologue as opro
+    docs = synth.spans_to_tuples(w.docs)
+    pos = oplan.positions(docs)
+    cu = oplan.cu_seqlens(docs)
+    heads = heads if heads is not None else list(range(w.num_heads))
+    flops = 0
+    rows_done = 0
+    t0 = time.perf_counter()
+    for h in heads:
+        xk = synth.bf16_bits_to_f64(t.k[:, h:h + 1])
+        kh = opro.qk_prologue(xk, t.gain_k.astype(np.float64), pos, w.eps)
+        v = synth.bf16_bits_to_f64(t.v[:, h:h + 1])
+        for r0 in range(0, w.S, chunk):
+            rows = np.arange(r0, min(w.S, r0 + chunk))
+            xq = synth.bf16_bits_to_f64(t.q[rows, h:h + 1])
+            qh = opro.qk_prologue(xq, t.gain_q.astype(np.float64), pos[rows], w.eps)
+            oatt.attention_rows(qh, kh, v, cu, w.softmax_scale, [0], rows)
+            d = oatt.doc_of_rows(cu, rows)
+            flops += int(4 * w.head_dim * np.sum(cu[d + 1] - cu[d]))
+            rows_done += rows.size
+            if time.perf_counter() - t0 > budget_s:
+                return flops, time.perf_counter() - t0, rows_done, heads[:heads.index(h) + 1]
+    return flops, time.perf_counter() - t0, rows_done, heads
+
+
+def cpu_cores():
+    return os.cpu_count() or 1
+
+
+def run_reference(args):
+    ws, rank, _ = dist_setup()
+    if rank != 0:
+        return 0
+    w = synth.config(WORKLOAD)
+    t = synth.make_tensors(w)
+    per_step = 6.0
+    for _ in range(args.warmup):
+        oracle_sample(w, t, 1.0)
+    flops_total, secs_total, rows_total = 0, 0.0, 0
+    for _ in range(args.steps):
+        f, s, r, _h = oracle_sample(w, t, per_step)
+        flops_total += f
+        secs_total += s
+        rows_total += r
+    value = flops_total / secs_total / 1e12
+    sample = (f"{args.steps} steps, each {per_step:.0f} s of fp64 numpy oracle (prologue + two-pass "
+              f"attention) over 512-row query chunks of head 0 onward; {rows_total} query rows x "
+              f"{w.S} keys in total")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": secs_total / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(w, {"sample": sample}),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# --------------------------------------------------------------- GPU leg ----
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"h3attn_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu), "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def traffic_for_current_kernel():
+    """DRAM bytes per forward launch from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    rec = json.load(open(TRAFFIC_FILE))
+    src = hashlib.sha256(open(FWD_SOURCE, "rb").read()).hexdigest()[:16]
+    return rec.get("dram_bytes_per_launch") if rec.get("kernel_source_sha256_16") == src else None
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    from packed_varlen_non_gb300 import build
+    from packed_varlen_non_gb300 import h3attn as H
+    from synth.device import bf16_to_torch
+
+    ws, rank, local = dist_setup()
+    if ws > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", torch.cuda.current_device())
+    build.ensure_built()
+
+    w = synth.config(WORKLOAD)
+    t = synth.make_tensors(w)
+    S, Hh = w.S, w.num_heads
+    W = Hh * 128
+    docs = synth.spans_to_tuples(w.docs)
+    stream = torch.cuda.Stream(device=dev)
+
+    t_plan0 = time.perf_counter()
+    plan = H.Plan(docs, Hh, stream=stream)
+    plan_ms = (time.perf_counter() - t_plan0) * 1e3
+
+    with torch.cuda.stream(stream):
+        q = bf16_to_torch(t.q, dev).view(S, W)
+        k = bf16_to_torch(t.k, dev).view(S, W)
+        v = bf16_to_torch(t.v, dev).view(S, W)
+        gq = torch.from_numpy(t.gain_q).to(dev)
+        gk = torch.from_numpy(t.gain_k).to(dev)
+        qh = torch.empty_like(q)
+        kh = torch.empty_like(k)
+        o = torch.empty_like(q)
+    stream.synchronize()
+    scale = w.softmax_scale
+
+    def step():
+        H.h3attn_qk_prologue(plan.handle, q, k, qh, kh, gq, gk, w.eps, stream=stream)
+        H.h3attn_forward(plan.handle, qh, kh, v, o, scale, None, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    stream.synchronize()
+    H.h3attn_get_device_error(plan.handle, stream=stream)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        H.h3attn_qk_prologue(plan.handle, q, k, qh, kh, gq, gk, w.eps, stream=stream)
+        ev[i][1].record(stream)
+        H.h3attn_forward(plan.handle, qh, kh, v, o, scale, None, stream=stream)
+        ev[i][2].record(stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    H.h3attn_get_device_error(plan.handle, stream=stream)
+    elapsed_ms = e0.elapsed_time(e1)
+    pro_ms = float(np.mean([ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]))
+    fwd_ms = float(np.mean([ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]))
+    checksum = float(o.float().abs().sum().item())  # consume the output
+    if ws > 1:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+
+    # end to end through the public API with host buffers: H2D of q, k, v from
+    # pinned memory, prologue, forward, D2H of o, every step
+    qp = torch.from_numpy(t.q.view(np.int16)).view(torch.bfloat16).view(S, W).pin_memory()
+    kp = torch.from_numpy(t.k.view(np.int16)).view(torch.bfloat16).view(S, W).pin_memory()
+    vp = torch.from_numpy(t.v.view(np.int16)).view(torch.bfloat16).view(S, W).pin_memory()
+    op = torch.empty((S, W), dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            q.copy_(qp, non_blocking=True)
+            k.copy_(kp, non_blocking=True)
+            v.copy_(vp, non_blocking=True)
+        step()
+        with torch.cuda.stream(stream):
+            op.copy_(o, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    stream.synchronize()
+    K2 = max(3, min(K, 50))
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(K2):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if ws > 1:
+        tt = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt.item())
+    H.h3attn_get_device_error(plan.handle, stream=stream)
+
+    pk = peaks()
+    flops = w.flops()
+    value = ws * flops * K / (elapsed_ms * 1e-3) / 1e12
+    fwd_tflops = flops / (fwd_ms * 1e-3) / 1e12
+    elem_bytes = S * W * 2
+    pro_bytes = 4 * elem_bytes + S * 48 * 8  # q, k read + written, rope table
+    pro_gbs = pro_bytes / (pro_ms * 1e-3) / 1e9
+
+    result = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline:
+            f, s, rows, hs = oracle_sample(w, t, args.cpu_seconds)
+            cpu = {"value": f / s / 1e12, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                   "sample": (f"fp64 numpy oracle (prologue + two-pass attention) on {rows} query rows x "
+                              f"{w.S} keys of heads {hs[0]}..{hs[-1]}, {s:.1f} s wall")}
+        result = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": K,
+            "warmup": max(3, args.warmup), "ms_per_step": elapsed_ms / K,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": workload_config(w, {"plan_ms": plan_ms, "replicas": ws,
+                                          "forward_ms": fwd_ms, "prologue_ms": pro_ms}),
+            "pct_of_peak": 100.0 * value / ws / pk["bf16_tflops"],
+            "forward_tflops": fwd_tflops,
+            "roofline": {"bound": "tensor", "kernel": "h3attn forward",
+                         "achieved": fwd_tflops, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": fwd_tflops / pk["bf16_tflops"],
+                         "peak_source": f"{pk['source']} dense bf16 (burst)",
+                         "traffic": traffic_for_current_kernel()},
+            "prologue": {"bound": "hbm", "achieved": pro_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                         "frac": pro_gbs / pk["hbm_gbs"], "algorithmic_bytes": pro_bytes},
+            "cpu_baseline": cpu,
+            "e2e": {"value": ws * flops * K2 / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+                    "h2d_bytes_per_step": 3 * elem_bytes, "d2h_bytes_per_step": elem_bytes,
+                    "ms_per_step": e2e_ms / K2},
+            "gpu_launches": 2 * K,
+            "clocks": clk,
+            "checksum": checksum,
+        }
+        print(json.dumps(result), flush=True)
+    plan.close()
+    if ws > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,179 @@
+/*
+ * h3attn -- packed varlen non-causal attention for the MiniMax-H3 DiT block,
+ * with its fused q/k prologue, on GB300 (sm_103a).
+ *
+ * What is computed (per DiT block, per head):
+ *   1. prologue on every q and k row: per-head RMSNorm with a gain, then the
+ *      3D (t, h, w) rotary embedding on head dims 0..95 (dims 96..127 pass
+ *      through);
+ *   2. attention that is bidirectional inside each cu_seqlens document of the
+ *      packed sequence and never crosses a document boundary.
+ *
+ * Pages defining it (page title, then section):
+ *   [PR26]  vllm.cpp PR #26 "feat(minimax-h3): port the MiniMax-H3 omni-modal
+ *           video+audio DiT" -- PR description (packed varlen NON-CAUSAL
+ *           attention with the per-document contract of a cu_seqlens varlen
+ *           flash-attention call, causal=false; the fp64 position grid gated
+ *           bit-exact, i*step + start), "The device-resident forward (W2b)"
+ *           (rotary = plain NeoX rotate_half with angles off the fp64 grid
+ *           through a per-row cos/sin cache; q/k RMSNorm), the encoder text
+ *           tower commit (per-head q/k RMSNorm);
+ *   [SPARK] "h3-spark" model card, "What this config does" (Q RMSNorm, then
+ *           rot96 RoPE, fused; byte-exact on default and non-default streams;
+ *           step-invariant rope caches).
+ *
+ * Conventions for every call:
+ *   - Tensors q, k, v, o are bf16, token-major "thd" packing: element
+ *     (token s, head h, dim d) sits at base + s*row_stride + h*128 + d
+ *     (strides in elements).  row_stride >= num_heads*128 lets q, k and v be
+ *     read straight out of a fused-qkv GEMM output [S, 3*H*128].
+ *   - All device pointers are caller-owned (the library never frees them)
+ *     and must be 16-byte aligned; row strides must be multiples of 8
+ *     elements.  Host pointers are caller-owned too.
+ *   - All compute calls are asynchronous on the given CUDA stream
+ *     (a cudaStream_t passed as void*; NULL = the legacy default stream) and
+ *     may be issued on any stream.  The library allocates no device memory on
+ *     the compute path; only h3attn_plan_create allocates, and
+ *     h3attn_plan_destroy frees.
+ *   - Functions never throw across the boundary.  Arguments are validated
+ *     before anything is launched; on failure nothing is launched, the
+ *     status says why, and h3attn_last_error() holds a message.
+ *   - A plan is used from one host thread at a time.
+ */
+#ifndef H3ATTN_H_
+#define H3ATTN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  H3ATTN_OK = 0,
+  H3ATTN_EINVAL = 1,        /* bad argument: null, misaligned, empty, out of range */
+  H3ATTN_EUNSUPPORTED = 2,  /* valid but not built: head_dim != 128, rope_dims != 96, not sm_103 */
+  H3ATTN_ENOMEM = 3,        /* device or host allocation failed (plan creation only) */
+  H3ATTN_ECUDA = 4,         /* a CUDA runtime/driver call failed; message has the CUDA error */
+  H3ATTN_ETIMEOUT = 5       /* a bounded device-side wait ran out (see h3attn_get_device_error) */
+} h3attn_status;
+
+/* Opaque plan: the packed layout of one request, built once and reused by
+ * every block and step ([SPARK] step-invariant rope caches). */
+typedef struct h3attn_plan* h3attn_plan_t;
+
+/* A grid of n_t x n_h x n_w tokens, ordered t-major then h, w fastest.  The
+ * position of token (i_t, i_h, i_w) on axis a is i_a*step[a] + start[a],
+ * evaluated in fp64 as one rounded product followed by one rounded sum
+ * ([PR26] PR description: numpy linspace(endpoint=False) order).  A 1D run
+ * (audio) is n_h = n_w = 1 with step {1, 0, 0}. */
+typedef struct {
+  int32_t n_t, n_h, n_w;
+  double start[3];
+  double step[3];
+} h3attn_span;
+
+/* A document: its spans concatenated in order.  Documents are packed back to
+ * back; cu_seqlens are the prefix sums of their lengths. */
+typedef struct {
+  const h3attn_span* spans;
+  int32_t n_spans;
+} h3attn_doc;
+
+typedef struct {
+  int32_t num_heads;   /* H >= 1 */
+  int32_t head_dim;    /* must be 128 */
+  int32_t rope_dims;   /* must be 96: 32 dims per axis (t, h, w), NeoX pairs j <-> j+48 */
+  double rope_base;    /* > 1; per-axis frequencies base^(-2k/32), k = 0..15 */
+} h3attn_plan_opts;
+
+/* Builds the plan on the host -- cu_seqlens (int32 [n_docs+1]), the fp64
+ * position grid [S,3], the fp32 cos/sin table [S,48] (angles in fp64) and the
+ * attention work list -- and uploads it to the current device on cuda_stream
+ * (the call synchronises that stream before returning).
+ * Errors: EINVAL for null docs/out, n_docs < 1, a document with no tokens, a
+ * span with a non-positive extent, non-finite start/step, S >= 2^31, H < 1;
+ * EUNSUPPORTED for head_dim != 128, rope_dims != 96 or a device that is not
+ * compute capability 10.3; ENOMEM / ECUDA from allocation or upload.
+ * On success *out owns device memory until h3attn_plan_destroy. */
+h3attn_status h3attn_plan_create(const h3attn_doc* docs, int32_t n_docs,
+                                 const h3attn_plan_opts* opts, void* cuda_stream,
+                                 h3attn_plan_t* out);
+
+/* Frees the plan's device and host memory (synchronises the device first).
+ * NULL is accepted and ignored. */
+h3attn_status h3attn_plan_destroy(h3attn_plan_t plan);
+
+/* Sizes of a plan; any output pointer may be NULL. */
+h3attn_status h3attn_plan_info(h3attn_plan_t plan, int64_t* total_tokens, int32_t* n_docs,
+                               int32_t* max_seqlen, int32_t* num_heads);
+
+/* Host copies of the plan's layout, for checking it: cu_seqlens into
+ * host_out[n_docs+1]; positions into host_out[S*3] (fp64, row-major [S,3],
+ * bit-exact); the rotary table into host_out[S*48*2] as (cos, sin) pairs of
+ * fp32, angle index a*16 + k for axis a in (t, h, w). */
+h3attn_status h3attn_plan_copy_cu_seqlens(h3attn_plan_t plan, int32_t* host_out);
+h3attn_status h3attn_plan_copy_positions(h3attn_plan_t plan, double* host_out);
+h3attn_status h3attn_plan_copy_rope_table(h3attn_plan_t plan, float* host_out);
+
+/* The q/k prologue ([SPARK] fused Q RMSNorm + rot96 RoPE; [PR26] W2b per-head
+ * RMSNorm and NeoX rotate_half from the per-row cos/sin cache).  For every
+ * token s, head h and tensor x in {q, k}:
+ *     r    = 1 / sqrt(mean_d x_d^2 + eps)
+ *     y_d  = x_d * r * gain[h*gain_head_stride + d]
+ *     j < 48:  out_j    = y_j cos(th_j) - y_{j+48} sin(th_j)
+ *              out_j+48 = y_{j+48} cos(th_j) + y_j sin(th_j)
+ *     d >= 96: out_d    = y_d
+ * with th from the plan's grid; fp32 arithmetic, one rounding to bf16.
+ * q_in/k_in: bf16 [S,H,128] with in_row_stride; q_out/k_out: bf16 with
+ * out_row_stride (in place is allowed when the pointers and strides are
+ * equal; partial overlap is not).  gain_q/gain_k: fp32 device arrays, [128]
+ * shared by all heads when gain_head_stride == 0, else [H, gain_head_stride].
+ * Errors: EINVAL for null/misaligned pointers, strides < H*128 or not
+ * multiples of 8, eps < 0 or not finite, partial overlap. */
+h3attn_status h3attn_qk_prologue(h3attn_plan_t plan, const void* q_in, const void* k_in,
+                                 int64_t in_row_stride, void* q_out, void* k_out,
+                                 int64_t out_row_stride, const float* gain_q,
+                                 const float* gain_k, int64_t gain_head_stride, float eps,
+                                 void* cuda_stream);
+
+/* Packed varlen non-causal attention ([PR26] PR description: per-document
+ * bidirectional attention, exactly a cu_seqlens varlen flash-attention call
+ * with causal=false).  For each head and each query token i of document
+ * [a, b):
+ *     s_ij = softmax_scale * <q_i, k_j>,   j in [a, b)
+ *     o_i  = sum_j softmax_j(s_ij) v_j     (bf16 out, fp32 accumulation)
+ *     lse[h*S + i] = ln sum_j exp(s_ij)    (only if lse_out != NULL)
+ * q, k, v: bf16 [S,H,128] with qkv_row_stride (the prologue's outputs, or a
+ * fused buffer); o: bf16 with o_row_stride, must not overlap q/k/v;
+ * lse_out: fp32 [H, S] device array or NULL.  Tensor-core kernel: TMA tiles,
+ * tcgen05 MMAs with TMEM accumulators, online softmax, a persistent grid over
+ * the plan's work list that never visits a cross-document tile.
+ * Errors: EINVAL for null/misaligned pointers, bad strides, o overlapping
+ * q/k/v, softmax_scale not finite or <= 0. */
+h3attn_status h3attn_forward(h3attn_plan_t plan, const void* q, const void* k, const void* v,
+                             int64_t qkv_row_stride, void* o, int64_t o_row_stride,
+                             float softmax_scale, float* lse_out, void* cuda_stream);
+
+/* Synchronises cuda_stream, then reads and clears the plan's device error
+ * word.  Returns OK, or ETIMEOUT if a kernel's bounded wait ran out since the
+ * last call (the kernel then stopped early and its outputs are invalid), or
+ * ECUDA if the stream reports an error. */
+h3attn_status h3attn_get_device_error(h3attn_plan_t plan, void* cuda_stream);
+
+/* Launches one CTA that waits on a shared-memory barrier nothing arrives on,
+ * through the same bounded wait the kernels use, with the given limit in
+ * nanoseconds (1e3 .. 1e10).  The kernel records the timeout and returns; the
+ * call synchronises and returns ETIMEOUT when the wait ran out as designed
+ * (OK would mean the bound is broken).  Exercises failure detection without
+ * faulting or hanging the GPU. */
+h3attn_status h3attn_selftest_bounded_wait(uint64_t timeout_ns, void* cuda_stream);
+
+/* Message for the last failing call on this host thread ("" if none). */
+const char* h3attn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* H3ATTN_H_ */

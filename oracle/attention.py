@@ -31,13 +31,14 @@ def doc_of_rows(cu: np.ndarray, rows: np.ndarray) -> np.ndarray:
     return np.searchsorted(cu, rows, side="right") - 1
 
 
-def attention_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, cu: np.ndarray,
+def attention_rows(q_sel: np.ndarray, k: np.ndarray, v: np.ndarray, cu: np.ndarray,
                    scale: float, heads, rows, chunk: int = 1024):
     """o [len(rows), len(heads), D] and lse [len(heads), len(rows)] for the
-    given query rows and heads.  q, k, v: fp64 [S, H, D]."""
+    given query rows and heads.  q_sel: fp64 [len(rows), H, D], the queries of
+    tokens ``rows``; k, v: fp64 [S, H, D]."""
     heads = np.asarray(list(heads), dtype=np.int64)
     rows = np.asarray(rows, dtype=np.int64)
-    D = q.shape[2]
+    D = k.shape[2]
     o = np.zeros((rows.size, heads.size, D), dtype=np.float64)
     lse = np.zeros((heads.size, rows.size), dtype=np.float64)
     docs = doc_of_rows(cu, rows)
@@ -49,7 +50,7 @@ def attention_rows(q: np.ndarray, k: np.ndarray, v: np.ndarray, cu: np.ndarray,
             vd = v[a:b, h, :]
             for c0 in range(0, sel.size, chunk):
                 ii = sel[c0:c0 + chunk]
-                s = scale * (q[rows[ii], h, :] @ kd.T)          # [n, L]
+                s = scale * (q_sel[ii, h, :] @ kd.T)            # [n, L]
                 m = np.max(s, axis=1, keepdims=True)            # pass 1: row max
                 e = np.exp(s - m)                               # pass 2: exponentials
                 l = np.sum(e, axis=1, keepdims=True)

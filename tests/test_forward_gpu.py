@@ -1,0 +1,136 @@
+"""Attention parity: the CUDA path (prologue + forward, through the C ABI)
+against the fp64 oracle on the five workloads and on edge cases; segment
+isolation must hold bit for bit."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from packed_varlen_non_gb300 import h3attn as H
+from synth.device import bf16_to_torch
+from tests.gpu_cases import (check_attention, docs_1d, oracle_reference, random_tensors,
+                             run_product, sample_rows)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("n", [1, 2])
+def test_workload_full_output(lib, n):
+    w = synth.config(n)
+    t = synth.make_tensors(w)
+    docs = synth.spans_to_tuples(w.docs)
+    r = run_product(docs, w.num_heads, t)
+    rows, o, lse, _ = oracle_reference(docs, t)
+    check_attention(r.o, o, r.lse, lse, f"config {n} end to end")
+    # the attention step alone, on the GPU prologue's own bf16 outputs
+    rows, o2, lse2, _ = oracle_reference(docs, t, q_hat=r.q_hat, k_hat=r.k_hat)
+    check_attention(r.o, o2, r.lse, lse2, f"config {n} attention only")
+
+
+@pytest.mark.parametrize("n", [3, 4, 5])
+def test_workload_sampled_rows(lib, n):
+    w = synth.config(n)
+    t = synth.make_tensors(w)
+    docs = synth.spans_to_tuples(w.docs)
+    r = run_product(docs, w.num_heads, t)
+    assert np.all(np.isfinite(r.o)), "non-finite output somewhere in the full tensor"
+    cu = np.concatenate([[0], np.cumsum(w.doc_lengths)])
+    rows = sample_rows(cu, seed=n)
+    _, o, lse, _ = oracle_reference(docs, t, rows=rows)
+    check_attention(r.o[rows], o, r.lse[:, rows], lse, f"config {n} sampled end to end")
+    _, o2, lse2, _ = oracle_reference(docs, t, rows=rows, q_hat=r.q_hat, k_hat=r.k_hat)
+    check_attention(r.o[rows], o2, r.lse[:, rows], lse2, f"config {n} sampled attention only")
+
+
+EDGE_LAYOUTS = {
+    "one_token": [1],
+    "single_tiles": [1, 7, 127, 128, 129],
+    "tile_boundaries": [255, 256, 257, 383, 384, 385],
+    "long_ragged": [1000, 3, 513],
+    "many_tiny": [int(x) for x in np.random.default_rng(11).integers(1, 40, 60)],
+}
+
+
+@pytest.mark.parametrize("name", sorted(EDGE_LAYOUTS))
+def test_edge_layouts(lib, name):
+    lens = EDGE_LAYOUTS[name]
+    docs = docs_1d(lens)
+    Hh = 3
+    t = random_tensors(sum(lens), Hh, seed=len(lens) * 7 + 1)
+    r = run_product(docs, Hh, t)
+    _, o, lse, _ = oracle_reference(docs, t, q_hat=r.q_hat, k_hat=r.k_hat)
+    check_attention(r.o, o, r.lse, lse, name)
+
+
+def test_one_token_documents_return_v(lib):
+    docs = docs_1d([1, 1, 1, 5, 1])
+    t = random_tensors(9, 2, seed=3)
+    r = run_product(docs, 2, t)
+    v = synth.bf16_bits_to_f64(t.v)
+    for i in (0, 1, 2, 8):
+        np.testing.assert_array_equal(r.o[i], v[i])
+
+
+def test_zero_gain_gives_document_mean(lib):
+    lens = [130, 77, 300]
+    docs = docs_1d(lens)
+    t = random_tensors(sum(lens), 2, seed=4)
+    t.gain_q[:] = 0.0
+    r = run_product(docs, 2, t)
+    v = synth.bf16_bits_to_f64(t.v)
+    a = 0
+    for L in lens:
+        mean = v[a:a + L].mean(axis=0)
+        check_attention(r.o[a:a + L], np.broadcast_to(mean, (L, 2, 128)), what=f"mean of doc len {L}")
+        a += L
+
+
+def test_segment_isolation_bit_exact(lib):
+    lens = [300, 517, 129]
+    docs = docs_1d(lens)
+    Hh = 3
+    t = random_tensors(sum(lens), Hh, seed=21)
+    r0 = run_product(docs, Hh, t)
+    t2 = synth.Tensors(t.q.copy(), t.k.copy(), t.v.copy(), t.gain_q, t.gain_k)
+    rng = np.random.default_rng(0)
+    for arr in (t2.q, t2.k, t2.v):
+        idx = 300 + rng.integers(0, 517, 20)
+        arr[idx] ^= np.uint16(0x0040)  # flip a mantissa bit of a few doc-2 tokens
+    r1 = run_product(docs, Hh, t2)
+    assert np.array_equal(r1.o_bits[:300], r0.o_bits[:300])
+    assert np.array_equal(r1.o_bits[817:], r0.o_bits[817:])
+    assert not np.array_equal(r1.o_bits[300:817], r0.o_bits[300:817])
+
+
+def test_streams_and_fused_layout_are_byte_identical(lib):
+    lens = [400, 250]
+    docs = docs_1d(lens)
+    t = random_tensors(650, 4, seed=8)
+    r0 = run_product(docs, 4, t)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        r1 = run_product(docs, 4, t, stream=s)
+    r2 = run_product(docs, 4, t, fused=True)
+    assert np.array_equal(r0.o_bits, r1.o_bits)
+    assert np.array_equal(r0.o_bits, r2.o_bits)
+    r3 = run_product(docs, 4, t, want_lse=False)
+    assert np.array_equal(r0.o_bits, r3.o_bits)
+
+
+def test_forward_rejects_bad_arguments(lib):
+    docs = docs_1d([64])
+    with H.Plan(docs, 2) as p:
+        q = torch.zeros(64, 256, dtype=torch.bfloat16, device="cuda")
+        k, v, o = torch.zeros_like(q), torch.zeros_like(q), torch.zeros_like(q)
+        for args in ((q, k, v, q), (q, k, v, v)):  # o aliases an input
+            with pytest.raises(H.H3AttnError) as e:
+                H.h3attn_forward(p.handle, *args, 0.1)
+            assert e.value.status == H.H3ATTN_EINVAL
+        with pytest.raises(H.H3AttnError):
+            H.h3attn_forward(p.handle, q, k, v, o, float("nan"))
+        with pytest.raises(H.H3AttnError):
+            H.h3attn_forward(p.handle, q.view(-1)[4:], k, v, o, 0.1, qkv_row_stride=256, o_row_stride=256)
+        with pytest.raises(H.H3AttnError):
+            H.h3attn_forward(p.handle, q, k, v, o, 0.1, qkv_row_stride=100, o_row_stride=256)
+        H.h3attn_forward(p.handle, q, k, v, o, 0.1)  # valid call still works
+        H.h3attn_get_device_error(p.handle)
