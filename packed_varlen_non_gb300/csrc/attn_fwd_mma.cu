@@ -237,8 +237,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_mma_kernel(ForwardArgs a
 
 }  // namespace
 
-cudaError_t launch_forward(const ForwardArgs& a, int num_sms, cudaStream_t stream,
-                           std::string* why) {
+cudaError_t launch_forward_mma(const ForwardArgs& a, int num_sms, cudaStream_t stream,
+                               std::string* why) {
   if (a.n_units == 0) return cudaSuccess;
   static bool configured = false;
   if (!configured) {

@@ -1,0 +1,453 @@
+// Packed varlen non-causal attention on the 5th-generation tensor cores.
+//
+// Pages: vllm.cpp PR #26 "feat(minimax-h3)", PR description (packed varlen
+// NON-CAUSAL attention: each query attends to every key of its own
+// cu_seqlens document and to nothing else -- a cu_seqlens varlen
+// flash-attention call with causal=false) and the warp-per-query-row commit
+// (online-softmax recurrence in f32; Q read once per query row).
+//
+// Design (one persistent CTA per SM, 10 warps):
+//   warp 9       TMA producer: Q tiles of the work unit, then the unit's
+//                document's K and V tiles through a 4-slot shared-memory ring.
+//   warp 8       MMA issuer (one thread) and TMEM owner: S_s = Q_s K_j^T and
+//                O_s += P_s V_j with tcgen05.mma, fp32 accumulators in TMEM.
+//   warps 0..3   softmax for query tile 0 (rows 0..127 of the unit),
+//   warps 4..7   softmax for query tile 1 (rows 128..255): one thread per
+//                query row reads its S row from TMEM, keeps the running max
+//                and sum in registers (no cross-thread reduction is needed
+//                since a thread owns a whole row), writes P as bf16 back into
+//                TMEM over its S columns, rescales its O row when the max has
+//                grown by more than 2^8, and at the end of the unit writes
+//                O / l and the log-sum-exp.
+// While one softmax group works on its tile, the tensor core runs the other
+// tile's MMAs (two-tile ping-pong).  A work unit (head, document, 256 query
+// rows) only visits its own document's key tiles; keys past the document end
+// in the last tile are masked to -inf, rows past it are never stored.
+//
+// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512); P_s is
+// bf16 packed two per column in the first 64 columns of S_s.
+//
+// Shared memory tiles are 128 rows x 64 bf16 (128 B per row, 128-byte TMA
+// swizzle); a 128 x 128 tile is two of them 16 KB apart.  Q and K are K-major
+// operands; V is the MN-major B operand of the PV product.
+//
+// Every mbarrier wait is bounded (mbar_wait_bounded): on expiry the CTA
+// raises an abort flag, records a timeout in the device error word, drains
+// its own copies and MMAs with bounded waits, frees TMEM and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "device_common.cuh"
+
+namespace h3 {
+
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kMmaWarp = 8;
+constexpr int kTmaWarp = 9;
+constexpr int kTileRows = 128;
+constexpr int kSlots = 4;
+constexpr uint32_t kHalfTileBytes = 128 * 128;        // 128 rows x 128 B
+constexpr uint32_t kTileBytes = 2 * kHalfTileBytes;   // 32 KB
+constexpr uint32_t kSmemQ = 0;                        // 2 tiles
+constexpr uint32_t kSmemKV = 2 * kTileBytes;          // kSlots tiles
+constexpr uint32_t kSmemBar = kSmemKV + kSlots * kTileBytes;
+// barriers: q_full[2] q_empty[2] kv_full[4] kv_empty[4] s_ready[2] p_ready[2] o_ready[2] drain
+constexpr int kNumBars = 2 + 2 + kSlots + kSlots + 2 + 2 + 2 + 1;
+constexpr uint32_t kSmemMisc = kSmemBar + kNumBars * 8;
+constexpr uint32_t kSmemBytes = kSmemMisc + 16;
+constexpr size_t kSmemAlloc = kSmemBytes + 1024;      // slack to align the base to 1 KB
+constexpr uint32_t kTmemCols = 512;
+constexpr uint64_t kTimeoutNs = 2000000000ull;        // 2 s
+constexpr float kRescaleThreshold = 8.0f;             // log2 units: rescale when max grows by > 2^8
+
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, M = 128, N = 128.
+constexpr uint32_t kIdescBase = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
+constexpr uint32_t kIdescQK = kIdescBase;             // A, B K-major
+constexpr uint32_t kIdescPV = kIdescBase | (1u << 16);  // B (V) MN-major
+
+// Shared-memory matrix descriptor with 128-byte swizzling.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+struct Bars {
+  uint32_t base;
+  __device__ uint32_t q_full(int s) const { return base + 8 * s; }
+  __device__ uint32_t q_empty(int s) const { return base + 8 * (2 + s); }
+  __device__ uint32_t kv_full(int i) const { return base + 8 * (4 + i); }
+  __device__ uint32_t kv_empty(int i) const { return base + 8 * (4 + kSlots + i); }
+  __device__ uint32_t s_ready(int s) const { return base + 8 * (4 + 2 * kSlots + s); }
+  __device__ uint32_t p_ready(int s) const { return base + 8 * (6 + 2 * kSlots + s); }
+  __device__ uint32_t o_ready(int s) const { return base + 8 * (8 + 2 * kSlots + s); }
+  __device__ uint32_t drain() const { return base + 8 * (10 + 2 * kSlots); }
+};
+
+struct UnitGeom {
+  int32_t q0, kv0, kv1, head, n_kv, n_st;
+};
+
+__device__ __forceinline__ UnitGeom unit_geom(const WorkUnit* units, int u) {
+  const int4 w = __ldg(reinterpret_cast<const int4*>(units) + u);
+  UnitGeom g;
+  g.q0 = w.x;
+  g.kv0 = w.y;
+  g.kv1 = w.z;
+  g.head = w.w;
+  g.n_kv = (w.z - w.y + kTileRows - 1) / kTileRows;
+  g.n_st = (w.x + kTileRows < w.z) ? 2 : 1;
+  return g;
+}
+
+// S (TMEM, 128 x 128 fp32) = Q (smem, K-major) * K^T (smem, K-major), 8 MMAs of K = 16.
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk) {
+    const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
+    dev::mma_ss(d_tmem, smem_desc(q_smem + off, 16, 1024), smem_desc(k_smem + off, 16, 1024), kIdescQK,
+                kk > 0 ? 1u : 0u);
+  }
+}
+
+// O (TMEM fp32) (+)= P (TMEM, bf16 pairs) * V (smem, MN-major), 8 MMAs of K = 16 keys.
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, bool acc) {
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    dev::mma_ts(d_tmem, p_tmem + kk * 8, smem_desc(v_smem + kk * 16 * 128, kHalfTileBytes, 1024), kIdescPV,
+                (acc || kk > 0) ? 1u : 0u);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, ForwardArgs a) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = dev::smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  unsigned char* smem = smem_raw + (sbase - raw);
+  const Bars bars{sbase + kSmemBar};
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSmemMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemMisc + 4);
+
+  const uint32_t warp = dev::warp_id_uniform();
+  const uint32_t lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int s = 0; s < 2; ++s) {
+      dev::mbar_init(bars.q_full(s), 1);
+      dev::mbar_init(bars.q_empty(s), 1);
+      dev::mbar_init(bars.s_ready(s), 1);
+      dev::mbar_init(bars.p_ready(s), kTileRows);
+      dev::mbar_init(bars.o_ready(s), 1);
+    }
+    for (int i = 0; i < kSlots; ++i) {
+      dev::mbar_init(bars.kv_full(i), 1);
+      dev::mbar_init(bars.kv_empty(i), 1);
+    }
+    dev::mbar_init(bars.drain(), 1);
+    dev::fence_barrier_init();
+  }
+  if (warp == kTmaWarp && lane == 0) {
+    dev::tma_prefetch_desc(&tm_q);
+    dev::tma_prefetch_desc(&tm_k);
+    dev::tma_prefetch_desc(&tm_v);
+  }
+  if (warp == kMmaWarp) {
+    dev::tmem_alloc(dev::smem_u32(tmem_slot), kTmemCols);
+    dev::tmem_relinquish();
+  }
+  dev::tc_fence_before();
+  __syncthreads();
+  dev::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------ TMA producer ----
+    if (lane == 0) {
+      const uint64_t pol_q = dev::policy_evict_first();
+      const uint64_t pol_kv = dev::policy_evict_last();
+      uint32_t kv_it = 0, q_it[2] = {0, 0};
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+        const UnitGeom g = unit_geom(a.units, u);
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          if (!ok || s >= g.n_st) break;
+          ok = dev::mbar_wait_bounded(bars.q_empty(s), (q_it[s] & 1) ^ 1, abort_flag, a.err, kTimeoutNs);
+          if (!ok) break;
+          const uint32_t dst = sbase + kSmemQ + s * kTileBytes;
+          dev::mbar_arrive_expect_tx(bars.q_full(s), kTileBytes);
+          const int32_t row = g.q0 + s * kTileRows;
+          dev::tma_load_2d(dst, &tm_q, bars.q_full(s), g.head * 128, row, pol_q);
+          dev::tma_load_2d(dst + kHalfTileBytes, &tm_q, bars.q_full(s), g.head * 128 + 64, row, pol_q);
+          ++q_it[s];
+        }
+        for (int j = 0; ok && j < g.n_kv; ++j) {
+          const int32_t row = g.kv0 + j * kTileRows;
+          for (int t = 0; t < 2; ++t) {  // K then V
+            const uint32_t slot = kv_it % kSlots;
+            ok = dev::mbar_wait_bounded(bars.kv_empty(slot), ((kv_it / kSlots) & 1) ^ 1, abort_flag, a.err,
+                                        kTimeoutNs);
+            if (!ok) break;
+            const uint32_t dst = sbase + kSmemKV + slot * kTileBytes;
+            const CUtensorMap* tm = t == 0 ? &tm_k : &tm_v;
+            dev::mbar_arrive_expect_tx(bars.kv_full(slot), kTileBytes);
+            dev::tma_load_2d(dst, tm, bars.kv_full(slot), g.head * 128, row, pol_kv);
+            dev::tma_load_2d(dst + kHalfTileBytes, tm, bars.kv_full(slot), g.head * 128 + 64, row, pol_kv);
+            ++kv_it;
+          }
+        }
+      }
+      if (!ok) {
+        // drain: wait (bounded) for every copy this thread issued into the ring and Q
+        for (uint32_t r = 0; r < kSlots && r < kv_it; ++r) {
+          const uint32_t it = kv_it - 1 - r;
+          dev::mbar_wait_bounded(bars.kv_full(it % kSlots), (it / kSlots) & 1, nullptr, nullptr, kTimeoutNs);
+        }
+#pragma unroll
+        for (int s = 0; s < 2; ++s)
+          if (q_it[s]) dev::mbar_wait_bounded(bars.q_full(s), (q_it[s] - 1) & 1, nullptr, nullptr, kTimeoutNs);
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    // -------------------------------------------------------- MMA issuer ----
+    if (lane == 0) {
+      uint32_t kv_it = 0, q_it0 = 0, q_it1 = 0, p_it0 = 0, p_it1 = 0;
+      bool ok = true;
+      bool issued = false;
+      for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+        const UnitGeom g = unit_geom(a.units, u);
+        ok = dev::mbar_wait_bounded(bars.q_full(0), q_it0 & 1, abort_flag, a.err, kTimeoutNs);
+        ++q_it0;
+        if (ok && g.n_st > 1) {
+          ok = dev::mbar_wait_bounded(bars.q_full(1), q_it1 & 1, abort_flag, a.err, kTimeoutNs);
+          ++q_it1;
+        }
+        const uint32_t k0 = kv_it % kSlots;
+        if (ok) ok = dev::mbar_wait_bounded(bars.kv_full(k0), (kv_it / kSlots) & 1, abort_flag, a.err, kTimeoutNs);
+        if (!ok) break;
+        dev::tc_fence_after();
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          if (s >= g.n_st) break;
+          issue_qk(tmem + s * 128, sbase + kSmemQ + s * kTileBytes, sbase + kSmemKV + k0 * kTileBytes);
+          dev::mma_commit(bars.s_ready(s));
+          if (g.n_kv == 1) dev::mma_commit(bars.q_empty(s));
+        }
+        dev::mma_commit(bars.kv_empty(k0));
+        issued = true;
+        for (int j = 0; j < g.n_kv; ++j) {
+          const uint32_t it_v = kv_it + 1, it_k = kv_it + 2;
+          const uint32_t vslot = it_v % kSlots, kslot = it_k % kSlots;
+          const bool more = j + 1 < g.n_kv;
+          ok = dev::mbar_wait_bounded(bars.kv_full(vslot), (it_v / kSlots) & 1, abort_flag, a.err, kTimeoutNs);
+          if (!ok) break;
+#pragma unroll
+          for (int s = 0; s < 2; ++s) {
+            if (s >= g.n_st) break;
+            uint32_t& p_it = s == 0 ? p_it0 : p_it1;
+            ok = dev::mbar_wait_bounded(bars.p_ready(s), p_it & 1, abort_flag, a.err, kTimeoutNs);
+            if (!ok) break;
+            ++p_it;
+            dev::tc_fence_after();
+            issue_pv(tmem + 256 + s * 128, tmem + s * 128, sbase + kSmemKV + vslot * kTileBytes, j > 0);
+            if (more) {
+              if (s == 0) {
+                ok = dev::mbar_wait_bounded(bars.kv_full(kslot), (it_k / kSlots) & 1, abort_flag, a.err,
+                                            kTimeoutNs);
+                if (!ok) break;
+                dev::tc_fence_after();
+              }
+              issue_qk(tmem + s * 128, sbase + kSmemQ + s * kTileBytes, sbase + kSmemKV + kslot * kTileBytes);
+              dev::mma_commit(bars.s_ready(s));
+              if (j + 2 == g.n_kv) dev::mma_commit(bars.q_empty(s));
+            } else {
+              dev::mma_commit(bars.o_ready(s));
+            }
+          }
+          if (!ok) break;
+          dev::mma_commit(bars.kv_empty(vslot));
+          if (more) dev::mma_commit(bars.kv_empty(kslot));
+          kv_it += 2;
+        }
+      }
+      if (!ok && issued) {
+        // drain: every MMA issued so far must finish before TMEM is freed
+        dev::mma_commit(bars.drain());
+        dev::mbar_wait_bounded(bars.drain(), 0, nullptr, nullptr, kTimeoutNs);
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- softmax ----
+    const int st = warp >> 2;            // query tile of this warpgroup
+    const uint32_t row_in_tile = threadIdx.x & 127;
+    const uint32_t lane_base = (warp & 3) * 32;
+    const uint32_t t_s = tmem + (lane_base << 16) + st * 128;        // S_s / P_s
+    const uint32_t t_o = tmem + (lane_base << 16) + 256 + st * 128;  // O_s
+    uint32_t s_it = 0, o_it = 0;
+    bool ok = true;
+    const float sl2 = a.scale_log2;
+    __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.o);
+    for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+      const UnitGeom g = unit_geom(a.units, u);
+      if (st >= g.n_st) continue;
+      float m_used = -INFINITY, l = 0.f;
+      for (int j = 0; j < g.n_kv; ++j) {
+        ok = dev::mbar_wait_bounded(bars.s_ready(st), s_it & 1, abort_flag, a.err, kTimeoutNs);
+        if (!ok) break;
+        ++s_it;
+        dev::tc_fence_after();
+        uint32_t r[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) dev::tmem_ld32(t_s + c * 32, r[c]);
+        dev::tmem_wait_ld();
+        float* sv = reinterpret_cast<float*>(&r[0][0]);
+        const int rem = g.kv1 - (g.kv0 + j * kTileRows);
+        if (rem < kTileRows) {
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= rem) sv[c] = -INFINITY;
+        }
+        float mx = sv[0];
+#pragma unroll
+        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, sv[c]);
+        const float m_new = mx * sl2;
+        // The running max only moves when it grows by more than 2^8; the O
+        // row is then rescaled after P is written (it is not read before the
+        // next PV product, which waits for p_ready).
+        float alpha = 1.f;
+        if (m_new > m_used + kRescaleThreshold) {
+          alpha = dev::ex2_approx(m_used - m_new);  // 0 on the first tile (m_used = -inf)
+          m_used = m_new;
+        }
+        const float neg = -m_used;
+        float rs = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t p[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float p0 = dev::ex2_approx(fmaf(sv[64 * h + 2 * c], sl2, neg));
+            const float p1 = dev::ex2_approx(fmaf(sv[64 * h + 2 * c + 1], sl2, neg));
+            rs += p0 + p1;
+            p[c] = dev::pack_bf16x2(p0, p1);
+          }
+          dev::tmem_st32(t_s + 32 * h, p);
+        }
+        l = l * alpha + rs;
+        if (alpha != 1.f && j > 0) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t ov[32];
+            dev::tmem_ld32(t_o + c * 32, ov);
+            dev::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            dev::tmem_st32(t_o + c * 32, ov);
+          }
+        }
+        dev::tmem_wait_st();
+        dev::tc_fence_before();
+        dev::mbar_arrive(bars.p_ready(st));
+      }
+      if (!ok) break;
+      ok = dev::mbar_wait_bounded(bars.o_ready(st), o_it & 1, abort_flag, a.err, kTimeoutNs);
+      if (!ok) break;
+      ++o_it;
+      dev::tc_fence_after();
+      const int32_t row = g.q0 + st * kTileRows + row_in_tile;
+      const bool valid = row < g.kv1;
+      const float inv = 1.f / l;
+      __nv_bfloat16* dst = og + (int64_t)row * a.o_stride + g.head * kHeadDim;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t ov[32];
+        dev::tmem_ld32(t_o + c * 32, ov);
+        dev::tmem_wait_ld();
+        if (valid) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            uint4 w;
+            w.x = dev::pack_bf16x2(__uint_as_float(ov[8 * e + 0]) * inv, __uint_as_float(ov[8 * e + 1]) * inv);
+            w.y = dev::pack_bf16x2(__uint_as_float(ov[8 * e + 2]) * inv, __uint_as_float(ov[8 * e + 3]) * inv);
+            w.z = dev::pack_bf16x2(__uint_as_float(ov[8 * e + 4]) * inv, __uint_as_float(ov[8 * e + 5]) * inv);
+            w.w = dev::pack_bf16x2(__uint_as_float(ov[8 * e + 6]) * inv, __uint_as_float(ov[8 * e + 7]) * inv);
+            *reinterpret_cast<uint4*>(dst + c * 32 + e * 8) = w;
+          }
+        }
+      }
+      if (valid && a.lse != nullptr)
+        a.lse[(int64_t)g.head * a.S + row] = (m_used + __log2f(l)) * 0.6931471805599453f;
+    }
+  }
+
+  dev::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    dev::tc_fence_after();
+    dev::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* base, int64_t S, int32_t H, int64_t stride, std::string* why) {
+  auto fn = encode_fn();
+  if (fn == nullptr) {
+    if (why) *why = "cuTensorMapEncodeTiled is unavailable";
+    return false;
+  }
+  cuuint64_t dims[2] = {(cuuint64_t)H * kHeadDim, (cuuint64_t)S};
+  cuuint64_t strides[1] = {(cuuint64_t)stride * 2};
+  cuuint32_t box[2] = {64, kTileRows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    if (why) *why = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string((int)r);
+    return false;
+  }
+  return true;
+}
+
+}  // namespace
+
+cudaError_t launch_forward(const ForwardArgs& a, int num_sms, cudaStream_t stream, std::string* why) {
+  if (a.n_units == 0) return cudaSuccess;
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, a.q, a.S, a.H, a.qkv_stride, why) || !make_map(&mk, a.k, a.S, a.H, a.qkv_stride, why) ||
+      !make_map(&mv, a.v, a.S, a.H, a.qkv_stride, why))
+    return cudaErrorInvalidValue;
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
+  });
+  if (attr != cudaSuccess) {
+    if (why) *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
+    return attr;
+  }
+  const int grid = a.n_units < num_sms ? a.n_units : num_sms;
+  attn_fwd_tc_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mq, mk, mv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace h3

@@ -182,6 +182,9 @@ def h3attn_qk_prologue(plan, q_in, k_in, q_out, k_out, gain_q, gain_k, eps: floa
                        stream=None):
     """Tensors: bf16 [S, H, 128]-shaped views (row stride taken from dim 0)
     or raw device pointers with explicit strides; gains fp32 on the device."""
+    for pair in ((q_in, k_in, in_row_stride), (q_out, k_out, out_row_stride)):
+        if pair[2] is None and not isinstance(pair[0], int) and pair[0].stride(0) != pair[1].stride(0):
+            raise ValueError("q and k must share one row stride on each side")
     _check(load().h3attn_qk_prologue(plan, _ptr(q_in), _ptr(k_in), _row_stride(q_in, in_row_stride),
                                      _ptr(q_out), _ptr(k_out), _row_stride(q_out, out_row_stride),
                                      _ptr(gain_q), _ptr(gain_k), int(gain_head_stride), float(eps),
@@ -190,6 +193,10 @@ def h3attn_qk_prologue(plan, q_in, k_in, q_out, k_out, gain_q, gain_k, eps: floa
 
 def h3attn_forward(plan, q, k, v, o, softmax_scale: float, lse=None, qkv_row_stride=None,
                    o_row_stride=None, stream=None):
+    if qkv_row_stride is None and not isinstance(q, int):
+        strides = {int(x.stride(0)) for x in (q, k, v)}
+        if len(strides) != 1:
+            raise ValueError(f"q, k and v must share one row stride (got {sorted(strides)})")
     _check(load().h3attn_forward(plan, _ptr(q), _ptr(k), _ptr(v), _row_stride(q, qkv_row_stride),
                                  _ptr(o), _row_stride(o, o_row_stride), float(softmax_scale),
                                  _ptr(lse), _stream(stream)), "h3attn_forward")

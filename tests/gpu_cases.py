@@ -67,8 +67,12 @@ def run_product(docs, num_heads, t: synth.Tensors, eps=1e-6, scale=None, stream=
             v = bf16_to_torch(t.v).view(S, W)
         gq = torch.from_numpy(t.gain_q).to(dev)
         gk = torch.from_numpy(t.gain_k).to(dev)
-        q_hat = torch.empty(S, W, dtype=torch.bfloat16, device=dev)
-        k_hat = torch.empty_like(q_hat)
+        if fused:
+            # prologue in place inside the fused buffer, so q, k and v share one row stride
+            q_hat, k_hat = q_in, k_in
+        else:
+            q_hat = torch.empty(S, W, dtype=torch.bfloat16, device=dev)
+            k_hat = torch.empty_like(q_hat)
         o = torch.full((S, W), float("nan"), dtype=torch.bfloat16, device=dev)
         lse = torch.full((num_heads, S), float("nan"), dtype=torch.float32, device=dev) if want_lse else None
         H.h3attn_qk_prologue(plan.handle, q_in, k_in, q_hat, k_hat, gq, gk, eps, stream=stream)
