@@ -34,7 +34,7 @@ import synth  # noqa: E402
 WORKLOAD = 3  # the S = 20,423 Ref2VA-shaped packed sequence
 METRIC = "packed varlen non-causal attention TFLOP/s and % of GB300 bf16 peak"
 UNIT = "TFLOP/s"
-FWD_SOURCE = os.path.join(ROOT, "packed_varlen_non_gb300", "csrc", "attn_fwd_mma.cu")
+FWD_SOURCE = os.path.join(ROOT, "packed_varlen_non_gb300", "csrc", "attn_fwd_tc.cu")
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_fwd_ref2va_traffic.json")
 
 

@@ -4,7 +4,6 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
-#include <cstdlib>
 #include <cstring>
 #include <new>
 
@@ -306,12 +305,7 @@ h3attn_status h3attn_forward(h3attn_plan_t plan, const void* q, const void* k, c
   ForwardArgs a{q, k, v, o, lse_out, qkv_row_stride, o_row_stride, S, H,
                 softmax_scale * 1.4426950408889634f, plan->d_units, plan->n_units, plan->d_err};
   std::string why;
-  static const bool use_mma = [] {
-    const char* v = getenv("H3ATTN_FORWARD_KERNEL");
-    return v != nullptr && strcmp(v, "mma") == 0;
-  }();
-  e = use_mma ? launch_forward_mma(a, plan->num_sms, static_cast<cudaStream_t>(cuda_stream), &why)
-              : launch_forward(a, plan->num_sms, static_cast<cudaStream_t>(cuda_stream), &why);
+  e = launch_forward(a, plan->num_sms, static_cast<cudaStream_t>(cuda_stream), &why);
   if (e != cudaSuccess) {
     if (!why.empty()) return fail(H3ATTN_ECUDA, "forward: %s", why.c_str());
     return cuda_fail(e, "forward launch");

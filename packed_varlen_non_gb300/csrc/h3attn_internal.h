@@ -96,8 +96,6 @@ struct ForwardArgs {
 };
 cudaError_t launch_forward(const ForwardArgs& a, int num_sms, cudaStream_t stream,
                            std::string* why);
-cudaError_t launch_forward_mma(const ForwardArgs& a, int num_sms, cudaStream_t stream,
-                               std::string* why);
 
 cudaError_t launch_selftest_bounded_wait(uint64_t timeout_ns, uint32_t* d_flag,
                                          cudaStream_t stream);
