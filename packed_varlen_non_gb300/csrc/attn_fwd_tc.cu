@@ -313,10 +313,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 128; ++c)
             if (c >= rem) sv[c] = -INFINITY;
         }
-        float mx = sv[0];
+        // row max with eight independent chains (a single chain would be a
+        // 128-deep dependency with only two softmax warps per sub-partition)
+        float mx8[8];
 #pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, sv[c]);
-        const float m_new = mx * sl2;
+        for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
+#pragma unroll
+        for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sv[c]);
+#pragma unroll
+        for (int w = 4; w > 0; w >>= 1)
+#pragma unroll
+          for (int i = 0; i < w; ++i) mx8[i] = fmaxf(mx8[i], mx8[i + w]);
+        const float m_new = mx8[0] * sl2;
         // The running max only moves when it grows by more than 2^8; the O
         // row is then rescaled after P is written (it is not read before the
         // next PV product, which waits for p_ready).
@@ -326,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           m_used = m_new;
         }
         const float neg = -m_used;
-        float rs = 0.f;
+        float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t p[32];
@@ -334,11 +342,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 32; ++c) {
             const float p0 = dev::ex2_approx(fmaf(sv[64 * h + 2 * c], sl2, neg));
             const float p1 = dev::ex2_approx(fmaf(sv[64 * h + 2 * c + 1], sl2, neg));
-            rs += p0 + p1;
+            rs8[c & 7] += p0 + p1;
             p[c] = dev::pack_bf16x2(p0, p1);
           }
           dev::tmem_st32(t_s + 32 * h, p);
         }
+        const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
         l = l * alpha + rs;
         if (alpha != 1.f && j > 0) {
 #pragma unroll
