@@ -35,7 +35,7 @@ WORKLOAD = 3  # the S = 20,423 Ref2VA-shaped packed sequence
 METRIC = "packed varlen non-causal attention TFLOP/s and % of GB300 bf16 peak"
 UNIT = "TFLOP/s"
 FWD_SOURCE = os.path.join(ROOT, "packed_varlen_non_gb300", "csrc", "attn_fwd_tc.cu")
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_fwd_ref2va_traffic.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_fwd_ref2va_traffic.txt")
 
 
 def peaks():
@@ -187,9 +187,15 @@ def traffic_for_current_kernel():
     taken on the current kernel source (else None)."""
     if not os.path.exists(TRAFFIC_FILE):
         return None
-    rec = json.load(open(TRAFFIC_FILE))
+    rec = {}
+    for line in open(TRAFFIC_FILE):
+        if ":" in line and not line.startswith("#"):
+            key, val = line.split(":", 1)
+            rec[key.strip()] = val.strip()
     src = hashlib.sha256(open(FWD_SOURCE, "rb").read()).hexdigest()[:16]
-    return rec.get("dram_bytes_per_launch") if rec.get("kernel_source_sha256_16") == src else None
+    if rec.get("kernel_source_sha256_16") != src:
+        return None
+    return int(rec["dram_bytes_per_launch"])
 
 
 def run_ours(args):
