@@ -56,8 +56,8 @@ constexpr uint32_t kTileBytes = 2 * kHalfTileBytes;   // 32 KB
 constexpr uint32_t kSmemQ = 0;                        // 2 tiles
 constexpr uint32_t kSmemKV = 2 * kTileBytes;          // kSlots tiles
 constexpr uint32_t kSmemBar = kSmemKV + kSlots * kTileBytes;
-// barriers: q_full[2] q_empty[2] kv_full[4] kv_empty[4] s_ready[2] p_ready[2] o_ready[2] drain
-constexpr int kNumBars = 2 + 2 + kSlots + kSlots + 2 + 2 + 2 + 1;
+// barriers: q_full[2] q_empty[2] kv_full[4] kv_empty[4] s_ready[2] p_ready[2][2] o_ready[2] drain
+constexpr int kNumBars = 2 + 2 + kSlots + kSlots + 2 + 4 + 2 + 1;
 constexpr uint32_t kSmemMisc = kSmemBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kSmemMisc + 16;
 constexpr size_t kSmemAlloc = kSmemBytes + 1024;      // slack to align the base to 1 KB
@@ -83,23 +83,26 @@ struct Bars {
   __device__ uint32_t kv_full(int i) const { return base + 8 * (4 + i); }
   __device__ uint32_t kv_empty(int i) const { return base + 8 * (4 + kSlots + i); }
   __device__ uint32_t s_ready(int s) const { return base + 8 * (4 + 2 * kSlots + s); }
-  __device__ uint32_t p_ready(int s) const { return base + 8 * (6 + 2 * kSlots + s); }
-  __device__ uint32_t o_ready(int s) const { return base + 8 * (8 + 2 * kSlots + s); }
-  __device__ uint32_t drain() const { return base + 8 * (10 + 2 * kSlots); }
+  __device__ uint32_t p_ready(int s, int h) const { return base + 8 * (6 + 2 * kSlots + 2 * s + h); }
+  __device__ uint32_t o_ready(int s) const { return base + 8 * (10 + 2 * kSlots + s); }
+  __device__ uint32_t drain() const { return base + 8 * (12 + 2 * kSlots); }
 };
 
 struct UnitGeom {
-  int32_t q0, kv0, kv1, head, n_kv, n_st;
+  int32_t q0, kv0, kv1, head, lo, hi, part, n_st;  // key tiles [lo, hi)
 };
 
 __device__ __forceinline__ UnitGeom unit_geom(const WorkUnit* units, int u) {
-  const int4 w = __ldg(reinterpret_cast<const int4*>(units) + u);
+  const int4 w = __ldg(reinterpret_cast<const int4*>(units) + 2 * u);
+  const int4 x = __ldg(reinterpret_cast<const int4*>(units) + 2 * u + 1);
   UnitGeom g;
   g.q0 = w.x;
   g.kv0 = w.y;
   g.kv1 = w.z;
   g.head = w.w;
-  g.n_kv = (w.z - w.y + kTileRows - 1) / kTileRows;
+  g.lo = x.x;
+  g.hi = x.y;
+  g.part = x.z;
   g.n_st = (w.x + kTileRows < w.z) ? 2 : 1;
   return g;
 }
@@ -114,12 +117,28 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint3
   }
 }
 
-// O (TMEM fp32) (+)= P (TMEM, bf16 pairs) * V (smem, MN-major), 8 MMAs of K = 16 keys.
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, bool acc) {
+// O (TMEM fp32) (+)= P (TMEM, bf16 pairs) * V (smem, MN-major) over keys
+// [64h, 64h + 64): 4 MMAs of K = 16 keys.
+__device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, int h, bool acc) {
 #pragma unroll
-  for (int kk = 0; kk < 8; ++kk)
+  for (int k4 = 0; k4 < 4; ++k4) {
+    const int kk = 4 * h + k4;
     dev::mma_ts(d_tmem, p_tmem + kk * 8, smem_desc(v_smem + kk * 16 * 128, kHalfTileBytes, 1024), kIdescPV,
                 (acc || kk > 0) ? 1u : 0u);
+  }
+}
+
+// One query row's 128 scores from TMEM (4 loads of 32 columns); keys past
+// the document end (column >= rem) are set to -inf.
+__device__ __forceinline__ void load_scores(uint32_t t_s, uint32_t (&r)[4][32], int rem) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) dev::tmem_ld32(t_s + c * 32, r[c]);
+  dev::tmem_wait_ld();
+  if (rem < kTileRows) {
+#pragma unroll
+    for (int c = 0; c < 128; ++c)
+      if (c >= rem) r[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -142,7 +161,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       dev::mbar_init(bars.q_full(s), 1);
       dev::mbar_init(bars.q_empty(s), 1);
       dev::mbar_init(bars.s_ready(s), 1);
-      dev::mbar_init(bars.p_ready(s), kTileRows);
+      dev::mbar_init(bars.p_ready(s, 0), kTileRows);
+      dev::mbar_init(bars.p_ready(s, 1), kTileRows);
       dev::mbar_init(bars.o_ready(s), 1);
     }
     for (int i = 0; i < kSlots; ++i) {
@@ -187,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           dev::tma_load_2d(dst + kHalfTileBytes, &tm_q, bars.q_full(s), g.head * 128 + 64, row, pol_q);
           ++q_it[s];
         }
-        for (int j = 0; ok && j < g.n_kv; ++j) {
+        for (int j = g.lo; ok && j < g.hi; ++j) {
           const int32_t row = g.kv0 + j * kTileRows;
           for (int t = 0; t < 2; ++t) {  // K then V
             const uint32_t slot = kv_it % kSlots;
@@ -237,25 +257,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (s >= g.n_st) break;
           issue_qk(tmem + s * 128, sbase + kSmemQ + s * kTileBytes, sbase + kSmemKV + k0 * kTileBytes);
           dev::mma_commit(bars.s_ready(s));
-          if (g.n_kv == 1) dev::mma_commit(bars.q_empty(s));
+          if (g.hi - g.lo == 1) dev::mma_commit(bars.q_empty(s));
         }
         dev::mma_commit(bars.kv_empty(k0));
         issued = true;
-        for (int j = 0; j < g.n_kv; ++j) {
+        for (int j = g.lo; j < g.hi; ++j) {
           const uint32_t it_v = kv_it + 1, it_k = kv_it + 2;
           const uint32_t vslot = it_v % kSlots, kslot = it_k % kSlots;
-          const bool more = j + 1 < g.n_kv;
+          const bool more = j + 1 < g.hi;
           ok = dev::mbar_wait_bounded(bars.kv_full(vslot), (it_v / kSlots) & 1, abort_flag, a.err, kTimeoutNs);
           if (!ok) break;
 #pragma unroll
           for (int s = 0; s < 2; ++s) {
             if (s >= g.n_st) break;
             uint32_t& p_it = s == 0 ? p_it0 : p_it1;
-            ok = dev::mbar_wait_bounded(bars.p_ready(s), p_it & 1, abort_flag, a.err, kTimeoutNs);
+            ok = dev::mbar_wait_bounded(bars.p_ready(s, 0), p_it & 1, abort_flag, a.err, kTimeoutNs);
+            if (!ok) break;
+            dev::tc_fence_after();
+            issue_pv_half(tmem + 256 + s * 128, tmem + s * 128, sbase + kSmemKV + vslot * kTileBytes, 0, j > g.lo);
+            ok = dev::mbar_wait_bounded(bars.p_ready(s, 1), p_it & 1, abort_flag, a.err, kTimeoutNs);
             if (!ok) break;
             ++p_it;
             dev::tc_fence_after();
-            issue_pv(tmem + 256 + s * 128, tmem + s * 128, sbase + kSmemKV + vslot * kTileBytes, j > 0);
+            issue_pv_half(tmem + 256 + s * 128, tmem + s * 128, sbase + kSmemKV + vslot * kTileBytes, 1, true);
             if (more) {
               if (s == 0) {
                 ok = dev::mbar_wait_bounded(bars.kv_full(kslot), (it_k / kSlots) & 1, abort_flag, a.err,
@@ -265,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               issue_qk(tmem + s * 128, sbase + kSmemQ + s * kTileBytes, sbase + kSmemKV + kslot * kTileBytes);
               dev::mma_commit(bars.s_ready(s));
-              if (j + 2 == g.n_kv) dev::mma_commit(bars.q_empty(s));
+              if (j + 2 == g.hi) dev::mma_commit(bars.q_empty(s));
             } else {
               dev::mma_commit(bars.o_ready(s));
             }
@@ -297,72 +321,72 @@ __global__ void __launch_bounds__(kThreads, 1)
       const UnitGeom g = unit_geom(a.units, u);
       if (st >= g.n_st) continue;
       float m_used = -INFINITY, l = 0.f;
-      for (int j = 0; j < g.n_kv; ++j) {
+      for (int j = g.lo; j < g.hi; ++j) {
         ok = dev::mbar_wait_bounded(bars.s_ready(st), s_it & 1, abort_flag, a.err, kTimeoutNs);
         if (!ok) break;
         ++s_it;
         dev::tc_fence_after();
         uint32_t r[4][32];
-#pragma unroll
-        for (int c = 0; c < 4; ++c) dev::tmem_ld32(t_s + c * 32, r[c]);
-        dev::tmem_wait_ld();
         float* sv = reinterpret_cast<float*>(&r[0][0]);
         const int rem = g.kv1 - (g.kv0 + j * kTileRows);
-        if (rem < kTileRows) {
+        load_scores(t_s, r, rem);
+        // Row max: eight independent chains of 3-input maxima (a single chain
+        // would be a 128-deep dependency with two softmax warps per
+        // sub-partition to hide it).
+        float mx[8];
 #pragma unroll
-          for (int c = 0; c < 128; ++c)
-            if (c >= rem) sv[c] = -INFINITY;
-        }
-        // row max with eight independent chains (a single chain would be a
-        // 128-deep dependency with only two softmax warps per sub-partition)
-        float mx8[8];
+        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(sv[i], sv[8 + i]);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
+        for (int c = 16; c < 128; c += 16)
 #pragma unroll
-        for (int c = 8; c < 128; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], sv[c]);
-#pragma unroll
-        for (int w = 4; w > 0; w >>= 1)
-#pragma unroll
-          for (int i = 0; i < w; ++i) mx8[i] = fmaxf(mx8[i], mx8[i + w]);
-        const float m_new = mx8[0] * sl2;
-        // The running max only moves when it grows by more than 2^8; the O
-        // row is then rescaled after P is written (it is not read before the
-        // next PV product, which waits for p_ready).
+          for (int i = 0; i < 8; ++i) mx[i] = dev::max3(mx[i], sv[c + i], sv[c + 8 + i]);
+        const float m_new =
+            dev::max3(dev::max3(mx[0], mx[1], mx[2]), dev::max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
+        // The reference max only moves when the row max grows by more than
+        // 2^8 (then O and l are rescaled; the final O / l is unchanged).
         float alpha = 1.f;
         if (m_new > m_used + kRescaleThreshold) {
           alpha = dev::ex2_approx(m_used - m_new);  // 0 on the first tile (m_used = -inf)
           m_used = m_new;
+          if (j > g.lo) {
+            // Rare: O must be rescaled before this tile's first PV reads it.
+            // The scores are reloaded afterwards so they are not held in
+            // registers across the rescale.
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t ov[32];
+              dev::tmem_ld32(t_o + c * 32, ov);
+              dev::tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+              dev::tmem_st32(t_o + c * 32, ov);
+            }
+            load_scores(t_s, r, rem);
+          }
         }
         const float neg = -m_used;
-        float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        // P in two halves of 64 keys: the MMA warp starts O += P V on the
+        // first half while the second is being exponentiated.
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t p[32];
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
-            const float p0 = dev::ex2_approx(fmaf(sv[64 * h + 2 * c], sl2, neg));
-            const float p1 = dev::ex2_approx(fmaf(sv[64 * h + 2 * c + 1], sl2, neg));
-            rs8[c & 7] += p0 + p1;
+            float x0, x1;
+            dev::fma2(x0, x1, sv[64 * h + 2 * c], sv[64 * h + 2 * c + 1], sl2, sl2, neg, neg);
+            const float p0 = dev::ex2_approx(x0), p1 = dev::ex2_approx(x1);
+            const int ai = 2 * (c & 3);
+            dev::add2(acc[ai], acc[ai + 1], acc[ai], acc[ai + 1], p0, p1);
             p[c] = dev::pack_bf16x2(p0, p1);
           }
           dev::tmem_st32(t_s + 32 * h, p);
+          dev::tmem_wait_st();
+          dev::tc_fence_before();
+          dev::mbar_arrive(bars.p_ready(st, h));
         }
-        const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+        const float rs = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
         l = l * alpha + rs;
-        if (alpha != 1.f && j > 0) {
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t ov[32];
-            dev::tmem_ld32(t_o + c * 32, ov);
-            dev::tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            dev::tmem_st32(t_o + c * 32, ov);
-          }
-        }
-        dev::tmem_wait_st();
-        dev::tc_fence_before();
-        dev::mbar_arrive(bars.p_ready(st));
       }
       if (!ok) break;
       ok = dev::mbar_wait_bounded(bars.o_ready(st), o_it & 1, abort_flag, a.err, kTimeoutNs);
@@ -371,6 +395,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       dev::tc_fence_after();
       const int32_t row = g.q0 + st * kTileRows + row_in_tile;
       const bool valid = row < g.kv1;
+      if (g.part >= 0) {
+        // A piece of a unit split along the keys: unnormalised O row, its
+        // reference max (log2 units) and sum, for the merge pass.
+        const size_t slot = (size_t)g.part * kUnitRows + st * kTileRows + row_in_tile;
+        float4* dst = reinterpret_cast<float4*>(a.part_o + slot * kHeadDim);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t ov[32];
+          dev::tmem_ld32(t_o + c * 32, ov);
+          dev::tmem_wait_ld();
+          if (valid) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              dst[c * 8 + e] = make_float4(__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
+                                           __uint_as_float(ov[4 * e + 2]), __uint_as_float(ov[4 * e + 3]));
+          }
+        }
+        if (valid) a.part_ml[slot] = make_float2(m_used, l);
+        continue;
+      }
       const float inv = 1.f / l;
       __nv_bfloat16* dst = og + (int64_t)row * a.o_stride + g.head * kHeadDim;
 #pragma unroll
@@ -401,6 +445,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     dev::tc_fence_after();
     dev::tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+// Combines the pieces of units split along the keys: one warp per query row,
+// four dims per lane.  With M = max_c m_c (log2 units):
+//   o = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c,  lse = (M + log2 l) ln 2.
+__global__ void __launch_bounds__(256) attn_merge_kernel(ForwardArgs a) {
+  const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  const int mu = warp_global / kUnitRows, r = warp_global % kUnitRows;
+  if (mu >= a.n_merges) return;
+  const MergeUnit m = a.merges[mu];
+  const int32_t row = m.q_row0 + r;
+  if (row >= m.kv_end) return;
+  float M = -INFINITY;
+  for (int c = 0; c < m.n_parts; ++c) M = fmaxf(M, a.part_ml[(size_t)(m.part0 + c) * kUnitRows + r].x);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float l = 0.f;
+  for (int c = 0; c < m.n_parts; ++c) {
+    const size_t slot = (size_t)(m.part0 + c) * kUnitRows + r;
+    const float2 ml = a.part_ml[slot];
+    const float w = dev::ex2_approx(ml.x - M);
+    const float4 o = reinterpret_cast<const float4*>(a.part_o + slot * kHeadDim)[lane];
+    acc.x = fmaf(w, o.x, acc.x);
+    acc.y = fmaf(w, o.y, acc.y);
+    acc.z = fmaf(w, o.z, acc.z);
+    acc.w = fmaf(w, o.w, acc.w);
+    l = fmaf(w, ml.y, l);
+  }
+  const float inv = 1.f / l;
+  __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.o) + (int64_t)row * a.o_stride + m.head * kHeadDim + 4 * lane;
+  *reinterpret_cast<uint2*>(dst) =
+      make_uint2(dev::pack_bf16x2(acc.x * inv, acc.y * inv), dev::pack_bf16x2(acc.z * inv, acc.w * inv));
+  if (lane == 0 && a.lse != nullptr) a.lse[(int64_t)m.head * a.S + row] = (M + __log2f(l)) * 0.6931471805599453f;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -456,6 +533,10 @@ cudaError_t launch_forward(const ForwardArgs& a, int num_sms, cudaStream_t strea
   }
   const int grid = a.n_units < num_sms ? a.n_units : num_sms;
   attn_fwd_tc_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mq, mk, mv, a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || a.n_merges == 0) return e;
+  const int64_t warps = (int64_t)a.n_merges * kUnitRows;
+  attn_merge_kernel<<<(int)((warps + 7) / 8), 256, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

@@ -82,6 +82,12 @@ void free_plan_device(Plan* p) {
   if (p->d_rope) cudaFree(p->d_rope);
   if (p->d_units) cudaFree(p->d_units);
   if (p->d_err) cudaFree(p->d_err);
+  if (p->d_merges) cudaFree(p->d_merges);
+  if (p->d_part_o) cudaFree(p->d_part_o);
+  if (p->d_part_ml) cudaFree(p->d_part_ml);
+  p->d_merges = nullptr;
+  p->d_part_o = nullptr;
+  p->d_part_ml = nullptr;
   p->d_cu = nullptr;
   p->d_rope = nullptr;
   p->d_units = nullptr;
@@ -118,19 +124,19 @@ h3attn_status h3attn_plan_create(const h3attn_doc* docs, int32_t n_docs,
   if (!std::isfinite(opts->rope_base) || !(opts->rope_base > 1.0))
     return fail(H3ATTN_EINVAL, "rope_base must be finite and > 1");
 
+  // Validate the layout on the host first (no device needed for EINVAL).
+  {
+    h3attn_plan probe;
+    std::string why;
+    try {
+      why = build_plan_host(docs, n_docs, *opts, 1, probe, /*validate_only=*/true);
+    } catch (const std::bad_alloc&) {
+      return fail(H3ATTN_ENOMEM, "host allocation failed while building the plan");
+    }
+    if (!why.empty()) return fail(H3ATTN_EINVAL, "%s", why.c_str());
+  }
   h3attn_plan* p = new (std::nothrow) h3attn_plan();
   if (p == nullptr) return fail(H3ATTN_ENOMEM, "host allocation failed");
-  std::string why;
-  try {
-    why = build_plan_host(docs, n_docs, *opts, *p);
-  } catch (const std::bad_alloc&) {
-    delete p;
-    return fail(H3ATTN_ENOMEM, "host allocation failed while building the plan");
-  }
-  if (!why.empty()) {
-    delete p;
-    return fail(H3ATTN_EINVAL, "%s", why.c_str());
-  }
 
   cudaError_t e = cudaGetDevice(&p->device);
   if (e != cudaSuccess) {
@@ -147,13 +153,24 @@ h3attn_status h3attn_plan_create(const h3attn_doc* docs, int32_t n_docs,
     return fail(H3ATTN_EUNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
                 dev, major, minor);
   }
+  // the work list is balanced for one persistent CTA per SM
+  try {
+    build_plan_host(docs, n_docs, *opts, p->num_sms, *p);
+  } catch (const std::bad_alloc&) {
+    delete p;
+    return fail(H3ATTN_ENOMEM, "host allocation failed while building the plan");
+  }
 
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   const size_t n_cu = p->cu_host.size(), n_rope = (size_t)p->S * kRopeHalf;
   if ((e = cudaMalloc(&p->d_cu, n_cu * sizeof(int32_t))) != cudaSuccess ||
       (e = cudaMalloc(&p->d_rope, n_rope * sizeof(float2))) != cudaSuccess ||
       (e = cudaMalloc(&p->d_units, p->units_host.size() * sizeof(WorkUnit))) != cudaSuccess ||
-      (e = cudaMalloc(&p->d_err, 16)) != cudaSuccess) {
+      (e = cudaMalloc(&p->d_err, 16)) != cudaSuccess ||
+      (p->n_parts > 0 &&
+       ((e = cudaMalloc(&p->d_merges, p->merges_host.size() * sizeof(MergeUnit))) != cudaSuccess ||
+        (e = cudaMalloc(&p->d_part_o, (size_t)p->n_parts * kUnitRows * kHeadDim * sizeof(float))) != cudaSuccess ||
+        (e = cudaMalloc(&p->d_part_ml, (size_t)p->n_parts * kUnitRows * sizeof(float2))) != cudaSuccess))) {
     free_plan_device(p);
     delete p;
     return e == cudaErrorMemoryAllocation ? fail(H3ATTN_ENOMEM, "cudaMalloc failed for the plan")
@@ -165,6 +182,9 @@ h3attn_status h3attn_plan_create(const h3attn_doc* docs, int32_t n_docs,
                            cudaMemcpyHostToDevice, st)) != cudaSuccess ||
       (e = cudaMemcpyAsync(p->d_units, p->units_host.data(), p->units_host.size() * sizeof(WorkUnit),
                            cudaMemcpyHostToDevice, st)) != cudaSuccess ||
+      (p->n_parts > 0 &&
+       (e = cudaMemcpyAsync(p->d_merges, p->merges_host.data(), p->merges_host.size() * sizeof(MergeUnit),
+                            cudaMemcpyHostToDevice, st)) != cudaSuccess) ||
       (e = cudaMemsetAsync(p->d_err, 0, 16, st)) != cudaSuccess ||
       (e = cudaStreamSynchronize(st)) != cudaSuccess) {
     free_plan_device(p);
@@ -303,7 +323,8 @@ h3attn_status h3attn_forward(h3attn_plan_t plan, const void* q, const void* k, c
   cudaError_t e = g.enter(plan->device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
   ForwardArgs a{q, k, v, o, lse_out, qkv_row_stride, o_row_stride, S, H,
-                softmax_scale * 1.4426950408889634f, plan->d_units, plan->n_units, plan->d_err};
+                softmax_scale * 1.4426950408889634f, plan->d_units, plan->n_units, plan->d_err,
+                plan->d_merges, (int32_t)plan->merges_host.size(), plan->d_part_o, plan->d_part_ml};
   std::string why;
   e = launch_forward(a, plan->num_sms, static_cast<cudaStream_t>(cuda_stream), &why);
   if (e != cudaSuccess) {

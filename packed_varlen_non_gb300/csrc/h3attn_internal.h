@@ -22,15 +22,42 @@ constexpr int kUnitRows = 256;      // query rows per attention work unit (two 1
 constexpr uint32_t kErrNone = 0;
 constexpr uint32_t kErrTimeout = 1;
 
-// One attention work unit: up to kUnitRows query rows of one head inside one
-// document; the key/value range is the whole document [kv_begin, kv_end).
+constexpr int kKeyTile = 128;      // key rows per tile
+
+// One attention work segment: up to kUnitRows query rows of one head inside
+// one document [kv_begin, kv_end), over that document's key tiles
+// [tile_lo, tile_hi) (all of them unless the unit was split along the keys to
+// balance the last wave).  part < 0: the segment writes the final output;
+// part >= 0: it writes unnormalised partial results to partial slot `part`
+// and a merge pass combines the slots of its unit.
 struct WorkUnit {
   int32_t q_row0;
   int32_t kv_begin;
   int32_t kv_end;
   int32_t head;
+  int32_t tile_lo;
+  int32_t tile_hi;
+  int32_t part;
+  int32_t pad;
 };
-static_assert(sizeof(WorkUnit) == 16, "WorkUnit is read as one 16-byte vector");
+static_assert(sizeof(WorkUnit) == 32, "WorkUnit is read as two 16-byte vectors");
+
+// A unit split along the keys: its partial slots [part0, part0 + n_parts).
+struct MergeUnit {
+  int32_t q_row0;
+  int32_t kv_end;
+  int32_t head;
+  int32_t part0;
+  int32_t n_parts;
+  int32_t pad[3];
+};
+static_assert(sizeof(MergeUnit) == 32, "MergeUnit is read as two 16-byte vectors");
+
+// Build the segment list for a grid of `grid` persistent CTAs: whole units in
+// round-robin rounds, then the last partial round's units split along their
+// key tiles so that every CTA gets one piece (plan.cpp).
+void build_segments(const std::vector<WorkUnit>& units, int grid, std::vector<WorkUnit>& segs,
+                    std::vector<MergeUnit>& merges, int32_t* n_parts);
 
 struct Plan {
   int device = -1;
@@ -44,18 +71,24 @@ struct Plan {
   std::vector<int32_t> cu_host;      // [n_docs + 1]
   std::vector<double> pos_host;      // [S, 3]
   std::vector<float> rope_host;      // [S, 48, 2] (cos, sin)
-  std::vector<WorkUnit> units_host;  // work list, longest documents first
+  std::vector<WorkUnit> units_host;  // segment list (see build_segments)
+  std::vector<MergeUnit> merges_host;
+  int32_t n_parts = 0;
 
   int32_t* d_cu = nullptr;
   float2* d_rope = nullptr;          // [S, 48] (cos, sin)
   WorkUnit* d_units = nullptr;
   int32_t n_units = 0;
+  MergeUnit* d_merges = nullptr;
+  float* d_part_o = nullptr;         // [n_parts, 256, 128] unnormalised O
+  float2* d_part_ml = nullptr;       // [n_parts, 256] (running max in log2 units, sum)
   uint32_t* d_err = nullptr;         // device error word
 };
 
 // Host-side plan construction (plan.cpp); returns an empty string or an error.
+// With validate_only, only the document/span checks run (no device needed).
 std::string build_plan_host(const h3attn_doc* docs, int32_t n_docs, const h3attn_plan_opts& opts,
-                            Plan& p);
+                            int grid, Plan& p, bool validate_only = false);
 
 // Error reporting for the C-ABI layer.
 h3attn_status fail(h3attn_status s, const char* fmt, ...);
@@ -93,6 +126,10 @@ struct ForwardArgs {
   const WorkUnit* units;
   int32_t n_units;
   uint32_t* err;
+  const MergeUnit* merges;    // may be null when n_merges == 0
+  int32_t n_merges;
+  float* part_o;
+  float2* part_ml;
 };
 cudaError_t launch_forward(const ForwardArgs& a, int num_sms, cudaStream_t stream,
                            std::string* why);

@@ -25,7 +25,7 @@ static bool finite3(const double* a) {
 }
 
 std::string build_plan_host(const h3attn_doc* docs, int32_t n_docs, const h3attn_plan_opts& opts,
-                            Plan& p) {
+                            int grid, Plan& p, bool validate_only) {
   p.n_docs = n_docs;
   p.num_heads = opts.num_heads;
   p.rope_base = opts.rope_base;
@@ -52,6 +52,7 @@ std::string build_plan_host(const h3attn_doc* docs, int32_t n_docs, const h3attn
   }
   p.S = S;
   p.max_seqlen = max_len;
+  if (validate_only) return "";
 
   // fp64 grid: per span, t-major then h, w fastest; one rounded product, one rounded sum.
   p.pos_host.resize((size_t)S * 3);
@@ -96,15 +97,87 @@ std::string build_plan_host(const h3attn_doc* docs, int32_t n_docs, const h3attn
   std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) {
     return (p.cu_host[a + 1] - p.cu_host[a]) > (p.cu_host[b + 1] - p.cu_host[b]);
   });
-  p.units_host.clear();
+  std::vector<WorkUnit> units;
   for (int32_t d : order) {
     const int32_t b = p.cu_host[d], e = p.cu_host[d + 1];
+    const int32_t n_kv = (e - b + kKeyTile - 1) / kKeyTile;
     for (int32_t h = 0; h < opts.num_heads; ++h)
-      for (int32_t r = b; r < e; r += kUnitRows) p.units_host.push_back(WorkUnit{r, b, e, h});
+      for (int32_t r = b; r < e; r += kUnitRows) units.push_back(WorkUnit{r, b, e, h, 0, n_kv, -1, 0});
   }
-  if (p.units_host.size() >= (size_t(1) << 31)) return "too many work units";
+  if (units.size() >= (size_t(1) << 30)) return "too many work units";
+  build_segments(units, grid, p.units_host, p.merges_host, &p.n_parts);
   p.n_units = (int32_t)p.units_host.size();
   return "";
+}
+
+// Cost of a unit in tile MMAs: key tiles x active query tiles.
+static int64_t unit_cost(const WorkUnit& u) {
+  const int64_t tiles = u.tile_hi - u.tile_lo;
+  return tiles * ((u.q_row0 + 128 < u.kv_end) ? 2 : 1);
+}
+
+void build_segments(const std::vector<WorkUnit>& units, int grid, std::vector<WorkUnit>& segs,
+                    std::vector<MergeUnit>& merges, int32_t* n_parts) {
+  // A persistent CTA takes segments c, c + grid, c + 2 grid, ...  Whole units
+  // fill the first floor(U / grid) rounds in list order (so the CTAs running
+  // at one moment share heads and documents, and their keys stay in L2).
+  // The L < grid units left for the last round are split along their key
+  // tiles into pieces of about equal cost, one piece per CTA, so the last
+  // round is as long as one piece instead of one whole unit.
+  segs.clear();
+  merges.clear();
+  *n_parts = 0;
+  const size_t G = grid > 0 ? (size_t)grid : 1;
+  const size_t full = units.size() / G * G;
+  segs.assign(units.begin(), units.begin() + full);
+  const size_t L = units.size() - full;
+  if (L == 0) return;
+  std::vector<int32_t> pieces(L, 1);
+  int64_t total = 0;
+  for (size_t i = 0; i < L; ++i) total += unit_cost(units[full + i]);
+  size_t used = L;
+  // proportional share of the grid, at most one piece per key tile
+  for (size_t i = 0; i < L; ++i) {
+    const WorkUnit& u = units[full + i];
+    const int64_t want = total > 0 ? (int64_t)(G * unit_cost(u) / total) : 1;
+    const int32_t cap = u.tile_hi - u.tile_lo;
+    const int32_t n = (int32_t)std::max<int64_t>(1, std::min<int64_t>(want, cap));
+    used += n - 1;
+    pieces[i] = n;
+  }
+  // hand out what is left to the units whose pieces are largest
+  while (used < G) {
+    size_t best = L;
+    double best_piece = 0.0;
+    for (size_t i = 0; i < L; ++i) {
+      const WorkUnit& u = units[full + i];
+      if (pieces[i] >= u.tile_hi - u.tile_lo) continue;
+      const double piece = (double)unit_cost(u) / pieces[i];
+      if (piece > best_piece) {
+        best_piece = piece;
+        best = i;
+      }
+    }
+    if (best == L) break;
+    ++pieces[best];
+    ++used;
+  }
+  for (size_t i = 0; i < L; ++i) {
+    const WorkUnit& u = units[full + i];
+    const int32_t n = pieces[i], tiles = u.tile_hi - u.tile_lo;
+    if (n == 1) {
+      segs.push_back(u);
+      continue;
+    }
+    merges.push_back(MergeUnit{u.q_row0, u.kv_end, u.head, *n_parts, n, {0, 0, 0}});
+    for (int32_t c = 0; c < n; ++c) {
+      WorkUnit piece = u;
+      piece.tile_lo = u.tile_lo + (int32_t)((int64_t)tiles * c / n);
+      piece.tile_hi = u.tile_lo + (int32_t)((int64_t)tiles * (c + 1) / n);
+      piece.part = (*n_parts)++;
+      segs.push_back(piece);
+    }
+  }
 }
 
 }  // namespace h3
