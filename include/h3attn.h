@@ -155,6 +155,34 @@ h3attn_status h3attn_forward(h3attn_plan_t plan, const void* q, const void* k, c
                              int64_t qkv_row_stride, void* o, int64_t o_row_stride,
                              float softmax_scale, float* lse_out, void* cuda_stream);
 
+/* Allocation-free forward.  The pages have no counterpart: this entry point
+ * exists for callers that may not allocate device memory -- code whose device
+ * memory is owned by a host framework's pool or arena (an engine plugin, a
+ * serving runtime that reserves all memory at start-up), or a latency-bound
+ * loop where a cudaMalloc would synchronise the device.  h3attn_plan_create
+ * allocates, so such callers cannot use h3attn_forward.
+ * Same computation and kernel as h3attn_forward, without a plan: cu_seqlens
+ * is a HOST int32 array [n_docs+1] (cu_seqlens[0] = 0, strictly increasing);
+ * the work list is built on the host and, with the kernel's error word, kept
+ * in one static device array of 1 MiB + 16 B that every GPU loading the
+ * library holds until the process exits.  At most 32768 work units (a unit is
+ * up to 256 query rows of one head in one document, so sum over documents of
+ * ceil(len/256) * num_heads <= 32768); larger layouts get EINVAL with a
+ * message.  q, k, v, o, lse_out and their rules are those of h3attn_forward,
+ * except that o must not share any byte range with q, k or v.
+ * Calls no cudaMalloc/cudaFree or other allocating routine.  The first call
+ * on a device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.  All
+ * calls share the array and it keeps the last call's contents: the work list
+ * is rewritten and the error word cleared on every call, and calls that
+ * overlap on the GPU (e.g. on two streams at once) race on it.  A bounded-wait
+ * timeout inside the kernel invalidates the output but is not reported here
+ * (there is no plan to hold it); use h3attn_forward where that matters. */
+h3attn_status h3attn_forward_noalloc(const int32_t* cu_seqlens, int32_t n_docs, int32_t num_heads,
+                                     const void* q, const void* k, const void* v,
+                                     int64_t qkv_row_stride, void* o, int64_t o_row_stride,
+                                     float softmax_scale, float* lse_out, void* cuda_stream);
+
 /* Synchronises cuda_stream, then reads and clears the plan's device error
  * word.  Returns OK, or ETIMEOUT if a kernel's bounded wait ran out since the
  * last call (the kernel then stopped early and its outputs are invalid), or

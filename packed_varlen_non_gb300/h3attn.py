@@ -54,6 +54,8 @@ _SIGS = {
                            c_void_p, c_void_p, c_int64, c_float, c_void_p],
     "h3attn_forward": [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_int64,
                        c_float, c_void_p, c_void_p],
+    "h3attn_forward_noalloc": [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_int64,
+                               c_void_p, c_int64, c_float, c_void_p, c_void_p],
     "h3attn_get_device_error": [c_void_p, c_void_p],
     "h3attn_selftest_bounded_wait": [c_uint64, c_void_p],
 }
@@ -200,6 +202,21 @@ def h3attn_forward(plan, q, k, v, o, softmax_scale: float, lse=None, qkv_row_str
     _check(load().h3attn_forward(plan, _ptr(q), _ptr(k), _ptr(v), _row_stride(q, qkv_row_stride),
                                  _ptr(o), _row_stride(o, o_row_stride), float(softmax_scale),
                                  _ptr(lse), _stream(stream)), "h3attn_forward")
+
+
+def h3attn_forward_noalloc(cu_seqlens, num_heads: int, q, k, v, o, softmax_scale: float, lse=None,
+                           qkv_row_stride=None, o_row_stride=None, stream=None):
+    """The allocation-free forward: cu_seqlens is a host int32 sequence
+    [n_docs + 1]; no plan and no device allocation (see include/h3attn.h)."""
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    if qkv_row_stride is None and not isinstance(q, int):
+        strides = {int(x.stride(0)) for x in (q, k, v)}
+        if len(strides) != 1:
+            raise ValueError(f"q, k and v must share one row stride (got {sorted(strides)})")
+    _check(load().h3attn_forward_noalloc(cu.ctypes.data, cu.size - 1, int(num_heads), _ptr(q), _ptr(k),
+                                         _ptr(v), _row_stride(q, qkv_row_stride), _ptr(o),
+                                         _row_stride(o, o_row_stride), float(softmax_scale), _ptr(lse),
+                                         _stream(stream)), "h3attn_forward_noalloc")
 
 
 def h3attn_get_device_error(plan, stream=None):
