@@ -275,32 +275,55 @@ def run_ours(args):
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)
         elapsed_ms = float(tt.item())
 
-    # end to end through the public API with host buffers: H2D of q, k, v from
-    # pinned memory, prologue, forward, D2H of o, every step
+    # End to end through the public API with host buffers: every step copies
+    # its q, k, v from pinned host memory to the device, runs the prologue and
+    # the forward, and copies o back to pinned host memory.  The copies run on
+    # their own streams with two device buffer sets, so step i's inputs move
+    # while step i-1 computes; all of them sit inside the timed region.
     qp = torch.from_numpy(t.q.view(np.int16)).view(torch.bfloat16).view(S, W).pin_memory()
     kp = torch.from_numpy(t.k.view(np.int16)).view(torch.bfloat16).view(S, W).pin_memory()
     vp = torch.from_numpy(t.v.view(np.int16)).view(torch.bfloat16).view(S, W).pin_memory()
     op = torch.empty((S, W), dtype=torch.bfloat16).pin_memory()
-
-    def e2e_step():
-        with torch.cuda.stream(stream):
-            q.copy_(qp, non_blocking=True)
-            k.copy_(kp, non_blocking=True)
-            v.copy_(vp, non_blocking=True)
-        step()
-        with torch.cuda.stream(stream):
-            op.copy_(o, non_blocking=True)
-
-    for _ in range(3):
-        e2e_step()
-    stream.synchronize()
+    bufs = [(q, k, v, o)] + [tuple(torch.empty_like(x) for x in (q, k, v, o))]
+    h2d = torch.cuda.Stream(device=dev)
+    d2h = torch.cuda.Stream(device=dev)
     K2 = max(3, min(K, 50))
+    n_e2e = K2 + 3
+    ev_in = [torch.cuda.Event() for _ in range(n_e2e)]
+    ev_comp = [torch.cuda.Event() for _ in range(n_e2e)]
+    ev_out = [torch.cuda.Event() for _ in range(n_e2e)]
+
+    def e2e_run(first, count):
+        for i in range(first, first + count):
+            bq, bk, bv, bo = bufs[i % 2]
+            if i - 2 >= first:
+                h2d.wait_event(ev_comp[i - 2])   # compute i-2 has read this buffer set
+            with torch.cuda.stream(h2d):
+                bq.copy_(qp, non_blocking=True)
+                bk.copy_(kp, non_blocking=True)
+                bv.copy_(vp, non_blocking=True)
+            ev_in[i].record(h2d)
+            stream.wait_event(ev_in[i])
+            if i - 2 >= first:
+                stream.wait_event(ev_out[i - 2])  # o of step i-2 has reached the host
+            H.h3attn_qk_prologue(plan.handle, bq, bk, qh, kh, gq, gk, w.eps, stream=stream)
+            H.h3attn_forward(plan.handle, qh, kh, bv, bo, scale, None, stream=stream)
+            ev_comp[i].record(stream)
+            d2h.wait_event(ev_comp[i])
+            with torch.cuda.stream(d2h):
+                op.copy_(bo, non_blocking=True)
+            ev_out[i].record(d2h)
+        stream.wait_event(ev_out[first + count - 1])
+        stream.wait_event(ev_in[first + count - 1])
+
+    e2e_run(0, 3)
+    torch.cuda.synchronize()
     if ws > 1:
         dist.barrier()
     torch.cuda.synchronize()
     e0.record(stream)
-    for _ in range(K2):
-        e2e_step()
+    h2d.wait_event(e0)
+    e2e_run(3, K2)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
@@ -345,7 +368,9 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": {"value": ws * flops * K2 / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
                     "h2d_bytes_per_step": 3 * elem_bytes, "d2h_bytes_per_step": elem_bytes,
-                    "ms_per_step": e2e_ms / K2},
+                    "ms_per_step": e2e_ms / K2,
+                    "method": "pinned host buffers; H2D of q, k, v and D2H of o every step on copy "
+                              "streams, double-buffered so copies overlap the neighbouring steps' compute"},
             "gpu_launches": 2 * K,
             "clocks": clk,
             "checksum": checksum,

@@ -56,8 +56,8 @@ constexpr uint32_t kTileBytes = 2 * kHalfTileBytes;   // 32 KB
 constexpr uint32_t kSmemQ = 0;                        // 2 tiles
 constexpr uint32_t kSmemKV = 2 * kTileBytes;          // kSlots tiles
 constexpr uint32_t kSmemBar = kSmemKV + kSlots * kTileBytes;
-// barriers: q_full[2] q_empty[2] kv_full[4] kv_empty[4] s_ready[2] p_ready[2][2] o_ready[2] drain
-constexpr int kNumBars = 2 + 2 + kSlots + kSlots + 2 + 4 + 2 + 1;
+// barriers: q_full[2] q_empty[2] kv_full[4] kv_empty[4] s_ready[2] p_ready[2] o_ready[2] drain
+constexpr int kNumBars = 2 + 2 + kSlots + kSlots + 2 + 2 + 2 + 1;
 constexpr uint32_t kSmemMisc = kSmemBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kSmemMisc + 16;
 constexpr size_t kSmemAlloc = kSmemBytes + 1024;      // slack to align the base to 1 KB
@@ -83,9 +83,9 @@ struct Bars {
   __device__ uint32_t kv_full(int i) const { return base + 8 * (4 + i); }
   __device__ uint32_t kv_empty(int i) const { return base + 8 * (4 + kSlots + i); }
   __device__ uint32_t s_ready(int s) const { return base + 8 * (4 + 2 * kSlots + s); }
-  __device__ uint32_t p_ready(int s, int h) const { return base + 8 * (6 + 2 * kSlots + 2 * s + h); }
-  __device__ uint32_t o_ready(int s) const { return base + 8 * (10 + 2 * kSlots + s); }
-  __device__ uint32_t drain() const { return base + 8 * (12 + 2 * kSlots); }
+  __device__ uint32_t p_ready(int s) const { return base + 8 * (6 + 2 * kSlots + s); }
+  __device__ uint32_t o_ready(int s) const { return base + 8 * (8 + 2 * kSlots + s); }
+  __device__ uint32_t drain() const { return base + 8 * (10 + 2 * kSlots); }
 };
 
 struct UnitGeom {
@@ -117,15 +117,12 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint3
   }
 }
 
-// O (TMEM fp32) (+)= P (TMEM, bf16 pairs) * V (smem, MN-major) over keys
-// [64h, 64h + 64): 4 MMAs of K = 16 keys.
-__device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, int h, bool acc) {
+// O (TMEM fp32) (+)= P (TMEM, bf16 pairs) * V (smem, MN-major), 8 MMAs of K = 16 keys.
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, bool acc) {
 #pragma unroll
-  for (int k4 = 0; k4 < 4; ++k4) {
-    const int kk = 4 * h + k4;
+  for (int kk = 0; kk < 8; ++kk)
     dev::mma_ts(d_tmem, p_tmem + kk * 8, smem_desc(v_smem + kk * 16 * 128, kHalfTileBytes, 1024), kIdescPV,
                 (acc || kk > 0) ? 1u : 0u);
-  }
 }
 
 // One query row's 128 scores from TMEM (4 loads of 32 columns); keys past
@@ -161,8 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       dev::mbar_init(bars.q_full(s), 1);
       dev::mbar_init(bars.q_empty(s), 1);
       dev::mbar_init(bars.s_ready(s), 1);
-      dev::mbar_init(bars.p_ready(s, 0), kTileRows);
-      dev::mbar_init(bars.p_ready(s, 1), kTileRows);
+      dev::mbar_init(bars.p_ready(s), kTileRows);
       dev::mbar_init(bars.o_ready(s), 1);
     }
     for (int i = 0; i < kSlots; ++i) {
@@ -271,15 +267,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int s = 0; s < 2; ++s) {
             if (s >= g.n_st) break;
             uint32_t& p_it = s == 0 ? p_it0 : p_it1;
-            ok = dev::mbar_wait_bounded(bars.p_ready(s, 0), p_it & 1, abort_flag, a.err, kTimeoutNs);
-            if (!ok) break;
-            dev::tc_fence_after();
-            issue_pv_half(tmem + 256 + s * 128, tmem + s * 128, sbase + kSmemKV + vslot * kTileBytes, 0, j > g.lo);
-            ok = dev::mbar_wait_bounded(bars.p_ready(s, 1), p_it & 1, abort_flag, a.err, kTimeoutNs);
+            ok = dev::mbar_wait_bounded(bars.p_ready(s), p_it & 1, abort_flag, a.err, kTimeoutNs);
             if (!ok) break;
             ++p_it;
             dev::tc_fence_after();
-            issue_pv_half(tmem + 256 + s * 128, tmem + s * 128, sbase + kSmemKV + vslot * kTileBytes, 1, true);
+            issue_pv(tmem + 256 + s * 128, tmem + s * 128, sbase + kSmemKV + vslot * kTileBytes, j > g.lo);
             if (more) {
               if (s == 0) {
                 ok = dev::mbar_wait_bounded(bars.kv_full(kslot), (it_k / kSlots) & 1, abort_flag, a.err,
@@ -325,14 +317,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = dev::mbar_wait_bounded(bars.s_ready(st), s_it & 1, abort_flag, a.err, kTimeoutNs);
         if (!ok) break;
         ++s_it;
+        __syncwarp();  // lanes leave the wait separately; the TMEM loads are warp-collective
         dev::tc_fence_after();
         uint32_t r[4][32];
         float* sv = reinterpret_cast<float*>(&r[0][0]);
         const int rem = g.kv1 - (g.kv0 + j * kTileRows);
         load_scores(t_s, r, rem);
-        // Row max: eight independent chains of 3-input maxima (a single chain
-        // would be a 128-deep dependency with two softmax warps per
-        // sub-partition to hide it).
+        // Row max: eight independent chains of 3-input maxima.
         float mx[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) mx[i] = fmaxf(sv[i], sv[8 + i]);
@@ -343,55 +334,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float m_new =
             dev::max3(dev::max3(mx[0], mx[1], mx[2]), dev::max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
         // The reference max only moves when the row max grows by more than
-        // 2^8 (then O and l are rescaled; the final O / l is unchanged).
+        // 2^8 (then O and l are rescaled; the final O / l is unchanged).  The
+        // O row is rescaled after P is written: the next PV waits for p_ready.
         float alpha = 1.f;
         if (m_new > m_used + kRescaleThreshold) {
           alpha = dev::ex2_approx(m_used - m_new);  // 0 on the first tile (m_used = -inf)
           m_used = m_new;
-          if (j > g.lo) {
-            // Rare: O must be rescaled before this tile's first PV reads it.
-            // The scores are reloaded afterwards so they are not held in
-            // registers across the rescale.
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              uint32_t ov[32];
-              dev::tmem_ld32(t_o + c * 32, ov);
-              dev::tmem_wait_ld();
-#pragma unroll
-              for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-              dev::tmem_st32(t_o + c * 32, ov);
-            }
-            load_scores(t_s, r, rem);
-          }
         }
         const float neg = -m_used;
-        // P in two halves of 64 keys: the MMA warp starts O += P V on the
-        // first half while the second is being exponentiated.
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t p[32];
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
+            // packed pair arithmetic: one f32x2 FMA for the exponents, one f32x2 add for the sums
             float x0, x1;
             dev::fma2(x0, x1, sv[64 * h + 2 * c], sv[64 * h + 2 * c + 1], sl2, sl2, neg, neg);
             const float p0 = dev::ex2_approx(x0), p1 = dev::ex2_approx(x1);
             const int ai = 2 * (c & 3);
-            dev::add2(acc[ai], acc[ai + 1], acc[ai], acc[ai + 1], p0, p1);
+            dev::add2(rs8[ai], rs8[ai + 1], rs8[ai], rs8[ai + 1], p0, p1);
             p[c] = dev::pack_bf16x2(p0, p1);
           }
           dev::tmem_st32(t_s + 32 * h, p);
-          dev::tmem_wait_st();
-          dev::tc_fence_before();
-          dev::mbar_arrive(bars.p_ready(st, h));
         }
-        const float rs = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+        const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
         l = l * alpha + rs;
+        // tcgen05.ld/st are warp-collective (.sync.aligned): the rescale runs
+        // for the whole warp when any of its rows needs it (alpha = 1 elsewhere).
+        if (j > g.lo && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t ov[32];
+            dev::tmem_ld32(t_o + c * 32, ov);
+            dev::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+            dev::tmem_st32(t_o + c * 32, ov);
+          }
+        }
+        dev::tmem_wait_st();
+        dev::tc_fence_before();
+        dev::mbar_arrive(bars.p_ready(st));
       }
       if (!ok) break;
       ok = dev::mbar_wait_bounded(bars.o_ready(st), o_it & 1, abort_flag, a.err, kTimeoutNs);
       if (!ok) break;
       ++o_it;
+      __syncwarp();
       dev::tc_fence_after();
       const int32_t row = g.q0 + st * kTileRows + row_in_tile;
       const bool valid = row < g.kv1;
@@ -442,6 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   dev::tc_fence_before();
   __syncthreads();
   if (warp == kMmaWarp) {
+    __syncwarp();  // lane 0 comes from the issue loop; dealloc is warp-collective
     dev::tc_fence_after();
     dev::tmem_dealloc(tmem, kTmemCols);
   }
