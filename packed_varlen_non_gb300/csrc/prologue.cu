@@ -72,56 +72,7 @@ __device__ __forceinline__ void norm_rope(float (&x)[8], const float* gain, cons
   }
 }
 
-struct RowIn {
-  uint4 q, k;
-  float c[8], s[8];
-  int64_t tok;
-  int head;
-};
-
-// Issue the loads of one (token, head) row: q and k (16 B per lane) and this
-// lane's eight (cos, sin) pairs.
-__device__ __forceinline__ void load_row(const PrologueArgs& a, const __nv_bfloat16* qi, const __nv_bfloat16* ki,
-                                         int64_t row, int lane16, RowIn& r) {
-  r.tok = row / a.H;
-  r.head = (int)(row - r.tok * a.H);
-  const int64_t in_off = r.tok * a.in_stride + r.head * kHeadDim + lane16 * 8;
-  r.q = __ldcs(reinterpret_cast<const uint4*>(qi + in_off));
-  r.k = __ldcs(reinterpret_cast<const uint4*>(ki + in_off));
-  if (lane16 < 12) {
-    const float4* t = reinterpret_cast<const float4*>(a.rope + r.tok * kRopeHalf + (lane16 % 6) * 8);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float4 cs = __ldg(t + i);  // (cos, sin) of two consecutive angles
-      r.c[2 * i] = cs.x;
-      r.s[2 * i] = cs.y;
-      r.c[2 * i + 1] = cs.z;
-      r.s[2 * i + 1] = cs.w;
-    }
-  } else {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      r.c[e] = 1.f;
-      r.s[e] = 0.f;
-    }
-  }
-}
-
-__device__ __forceinline__ void finish_row(const PrologueArgs& a, __nv_bfloat16* qo, __nv_bfloat16* ko,
-                                           const RowIn& r, int lane16, unsigned mask) {
-  float xq[8], xk[8];
-  unpack8(r.q, xq);
-  unpack8(r.k, xk);
-  norm_rope(xq, a.gain_q + r.head * a.gain_head_stride, r.c, r.s, lane16, mask, a.eps);
-  norm_rope(xk, a.gain_k + r.head * a.gain_head_stride, r.c, r.s, lane16, mask, a.eps);
-  const int64_t out_off = r.tok * a.out_stride + r.head * kHeadDim + lane16 * 8;
-  __stcs(reinterpret_cast<uint4*>(qo + out_off), pack8(xq));
-  __stcs(reinterpret_cast<uint4*>(ko + out_off), pack8(xk));
-}
-
-// Each 16-lane group takes two rows per iteration (stride apart) and issues
-// all of their loads before using any, so twice the bytes are in flight.
-__global__ void __launch_bounds__(kThreads, 2) qk_prologue_kernel(PrologueArgs a) {
+__global__ void __launch_bounds__(kThreads) qk_prologue_kernel(PrologueArgs a) {
   const int lane16 = threadIdx.x & 15;
   const unsigned mask = 0xffffu << (threadIdx.x & 16);
   const int64_t n_rows = a.S * a.H;
@@ -132,13 +83,39 @@ __global__ void __launch_bounds__(kThreads, 2) qk_prologue_kernel(PrologueArgs a
   __nv_bfloat16* ko = static_cast<__nv_bfloat16*>(a.k_out);
 #pragma unroll 1
   for (int64_t row = (int64_t)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 4); row < n_rows;
-       row += 2 * step) {
-    const bool second = row + step < n_rows;  // uniform within the 16-lane group
-    RowIn r0, r1;
-    load_row(a, qi, ki, row, lane16, r0);
-    if (second) load_row(a, qi, ki, row + step, lane16, r1);
-    finish_row(a, qo, ko, r0, lane16, mask);
-    if (second) finish_row(a, qo, ko, r1, lane16, mask);
+       row += step) {
+    const int64_t tok = row / a.H;
+    const int head = (int)(row - tok * a.H);
+    const int64_t in_off = tok * a.in_stride + head * kHeadDim + lane16 * 8;
+    const uint4 qraw = __ldcs(reinterpret_cast<const uint4*>(qi + in_off));
+    const uint4 kraw = __ldcs(reinterpret_cast<const uint4*>(ki + in_off));
+    float c[8], s[8];
+    if (lane16 < 12) {
+      const float4* t =
+          reinterpret_cast<const float4*>(a.rope + tok * kRopeHalf + (lane16 % 6) * 8);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 cs = __ldg(t + i);  // (cos, sin) of two consecutive angles
+        c[2 * i] = cs.x;
+        s[2 * i] = cs.y;
+        c[2 * i + 1] = cs.z;
+        s[2 * i + 1] = cs.w;
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        c[e] = 1.f;
+        s[e] = 0.f;
+      }
+    }
+    float xq[8], xk[8];
+    unpack8(qraw, xq);
+    unpack8(kraw, xk);
+    norm_rope(xq, a.gain_q + head * a.gain_head_stride, c, s, lane16, mask, a.eps);
+    norm_rope(xk, a.gain_k + head * a.gain_head_stride, c, s, lane16, mask, a.eps);
+    const int64_t out_off = tok * a.out_stride + head * kHeadDim + lane16 * 8;
+    __stcs(reinterpret_cast<uint4*>(qo + out_off), pack8(xq));
+    __stcs(reinterpret_cast<uint4*>(ko + out_off), pack8(xk));
   }
 }
 
@@ -147,16 +124,12 @@ __global__ void __launch_bounds__(kThreads, 2) qk_prologue_kernel(PrologueArgs a
 cudaError_t launch_qk_prologue(const PrologueArgs& a, int num_sms, cudaStream_t stream) {
   const int64_t n_rows = a.S * a.H;
   if (n_rows == 0) return cudaSuccess;
-  // One wave of resident blocks (grid-stride loop), or fewer when there is
-  // less work: each block covers 2 x 16 rows per iteration.
-  static int per_sm = 0;
-  if (per_sm == 0) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, qk_prologue_kernel, kThreads, 0) != cudaSuccess ||
-        per_sm < 1)
-      per_sm = 1;
-  }
-  const int64_t want = (n_rows + 2 * kRowsPerBlock - 1) / (2 * kRowsPerBlock);
-  const int64_t full = (int64_t)num_sms * per_sm;
+  // 8 blocks of 256 threads per SM (at 64 registers, 4 of them are resident at
+  // a time; the grid-stride loop keeps the rest queued behind), or fewer
+  // when there is less work.  A variant with two rows of loads in flight per
+  // lane group and a single resident wave measured slower (3.7 vs 4.4 TB/s).
+  const int64_t want = (n_rows + kRowsPerBlock - 1) / kRowsPerBlock;
+  const int64_t full = (int64_t)num_sms * 8;
   const int grid = (int)(want < full ? want : full);
   qk_prologue_kernel<<<grid, kThreads, 0, stream>>>(a);
   return cudaGetLastError();
