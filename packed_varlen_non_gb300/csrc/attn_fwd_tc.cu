@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
           if (!ok || s >= g.n_st) break;
-          ok = dev::mbar_wait_bounded(bars.q_empty(s), (q_it[s] & 1) ^ 1, abort_flag, a.err, kTimeoutNs);
+          ok = dev::mbar_wait(bars.q_empty(s), (q_it[s] & 1) ^ 1, abort_flag, a.err, kTimeoutNs);
           if (!ok) break;
           const uint32_t dst = sbase + kSmemQ + s * kTileBytes;
           dev::mbar_arrive_expect_tx(bars.q_full(s), kTileBytes);
@@ -207,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int32_t row = g.kv0 + j * kTileRows;
           for (int t = 0; t < 2; ++t) {  // K then V
             const uint32_t slot = kv_it % kSlots;
-            ok = dev::mbar_wait_bounded(bars.kv_empty(slot), ((kv_it / kSlots) & 1) ^ 1, abort_flag, a.err,
+            ok = dev::mbar_wait(bars.kv_empty(slot), ((kv_it / kSlots) & 1) ^ 1, abort_flag, a.err,
                                         kTimeoutNs);
             if (!ok) break;
             const uint32_t dst = sbase + kSmemKV + slot * kTileBytes;
@@ -238,14 +238,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool issued = false;
       for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
         const UnitGeom g = unit_geom(a.units, u);
-        ok = dev::mbar_wait_bounded(bars.q_full(0), q_it0 & 1, abort_flag, a.err, kTimeoutNs);
+        ok = dev::mbar_wait(bars.q_full(0), q_it0 & 1, abort_flag, a.err, kTimeoutNs);
         ++q_it0;
         if (ok && g.n_st > 1) {
-          ok = dev::mbar_wait_bounded(bars.q_full(1), q_it1 & 1, abort_flag, a.err, kTimeoutNs);
+          ok = dev::mbar_wait(bars.q_full(1), q_it1 & 1, abort_flag, a.err, kTimeoutNs);
           ++q_it1;
         }
         const uint32_t k0 = kv_it % kSlots;
-        if (ok) ok = dev::mbar_wait_bounded(bars.kv_full(k0), (kv_it / kSlots) & 1, abort_flag, a.err, kTimeoutNs);
+        if (ok) ok = dev::mbar_wait(bars.kv_full(k0), (kv_it / kSlots) & 1, abort_flag, a.err, kTimeoutNs);
         if (!ok) break;
         dev::tc_fence_after();
 #pragma unroll
@@ -261,20 +261,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t it_v = kv_it + 1, it_k = kv_it + 2;
           const uint32_t vslot = it_v % kSlots, kslot = it_k % kSlots;
           const bool more = j + 1 < g.hi;
-          ok = dev::mbar_wait_bounded(bars.kv_full(vslot), (it_v / kSlots) & 1, abort_flag, a.err, kTimeoutNs);
+          ok = dev::mbar_wait(bars.kv_full(vslot), (it_v / kSlots) & 1, abort_flag, a.err, kTimeoutNs);
           if (!ok) break;
 #pragma unroll
           for (int s = 0; s < 2; ++s) {
             if (s >= g.n_st) break;
             uint32_t& p_it = s == 0 ? p_it0 : p_it1;
-            ok = dev::mbar_wait_bounded(bars.p_ready(s), p_it & 1, abort_flag, a.err, kTimeoutNs);
+            ok = dev::mbar_wait(bars.p_ready(s), p_it & 1, abort_flag, a.err, kTimeoutNs);
             if (!ok) break;
             ++p_it;
             dev::tc_fence_after();
             issue_pv(tmem + 256 + s * 128, tmem + s * 128, sbase + kSmemKV + vslot * kTileBytes, j > g.lo);
             if (more) {
               if (s == 0) {
-                ok = dev::mbar_wait_bounded(bars.kv_full(kslot), (it_k / kSlots) & 1, abort_flag, a.err,
+                ok = dev::mbar_wait(bars.kv_full(kslot), (it_k / kSlots) & 1, abort_flag, a.err,
                                             kTimeoutNs);
                 if (!ok) break;
                 dev::tc_fence_after();
@@ -314,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (st >= g.n_st) continue;
       float m_used = -INFINITY, l = 0.f;
       for (int j = g.lo; j < g.hi; ++j) {
-        ok = dev::mbar_wait_bounded(bars.s_ready(st), s_it & 1, abort_flag, a.err, kTimeoutNs);
+        ok = dev::mbar_wait(bars.s_ready(st), s_it & 1, abort_flag, a.err, kTimeoutNs);
         if (!ok) break;
         ++s_it;
         __syncwarp();  // lanes leave the wait separately; the TMEM loads are warp-collective
@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         dev::mbar_arrive(bars.p_ready(st));
       }
       if (!ok) break;
-      ok = dev::mbar_wait_bounded(bars.o_ready(st), o_it & 1, abort_flag, a.err, kTimeoutNs);
+      ok = dev::mbar_wait(bars.o_ready(st), o_it & 1, abort_flag, a.err, kTimeoutNs);
       if (!ok) break;
       ++o_it;
       __syncwarp();

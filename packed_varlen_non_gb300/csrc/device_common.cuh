@@ -94,6 +94,16 @@ static __device__ __noinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t par
   }
 }
 
+// Inline fast path for the hot waits: one try_wait before falling back to the
+// out-of-line bounded wait.  Calling the bounded wait on an already-complete
+// phase costs ~450-600 cycles in the MMA-issuing thread on GB300 (an inline
+// poll ~190), and that thread paces the tensor core.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                          uint32_t* err_word, uint64_t timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_bounded(bar, parity, abort, err_word, timeout_ns);
+}
+
 // ----------------------------------------------------------------- TMA ----
 
 __device__ __forceinline__ void tma_prefetch_desc(const void* desc) {
