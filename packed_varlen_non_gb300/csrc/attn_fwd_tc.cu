@@ -8,7 +8,9 @@
 //
 // Design (one persistent CTA per SM, 10 warps):
 //   warp 9       TMA producer: Q tiles of the work unit, then the unit's
-//                document's K and V tiles through a 4-slot shared-memory ring.
+//                document's K and V tiles through a 4-slot shared-memory ring,
+//                V(j) and the next K tile loaded as one group behind one
+//                barrier (one readiness poll and one release per key tile).
 //   warp 8       MMA issuer (one thread) and TMEM owner: S_s = Q_s K_j^T and
 //                O_s += P_s V_j with tcgen05.mma, fp32 accumulators in TMEM.
 //   warps 0..3   softmax for query tile 0 (rows 0..127 of the unit),
@@ -107,6 +109,13 @@ __device__ __forceinline__ UnitGeom unit_geom(const WorkUnit* units, int u) {
   return g;
 }
 
+// One 128-row tile of K or V (two 64-column boxes) into a ring slot.
+__device__ __forceinline__ void load_kv_tile(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int head,
+                                             int32_t row, uint64_t pol) {
+  dev::tma_load_2d(dst, tm, bar, head * 128, row, pol);
+  dev::tma_load_2d(dst + kHalfTileBytes, tm, bar, head * 128 + 64, row, pol);
+}
+
 // S (TMEM, 128 x 128 fp32) = Q (smem, K-major) * K^T (smem, K-major), 8 MMAs of K = 16.
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
 #pragma unroll
@@ -187,7 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint64_t pol_q = dev::policy_evict_first();
       const uint64_t pol_kv = dev::policy_evict_last();
-      uint32_t kv_it = 0, q_it[2] = {0, 0};
+      uint32_t grp = 0, q_it[2] = {0, 0};
       bool ok = true;
       for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
         const UnitGeom g = unit_geom(a.units, u);
@@ -203,27 +212,44 @@ __global__ void __launch_bounds__(kThreads, 1)
           dev::tma_load_2d(dst + kHalfTileBytes, &tm_q, bars.q_full(s), g.head * 128 + 64, row, pol_q);
           ++q_it[s];
         }
+        // Key/value groups: group 0 is the first unit's first K tile (ring slot
+        // 0); group n >= 1 is V(j) with the next K tile -- K(j+1), or the next
+        // unit's first K tile -- in slots (2n-1) % 4 and 2n % 4, one full and
+        // one empty barrier (index n & 1) for both.
+        if (u == (int)blockIdx.x) {
+          ok = dev::mbar_wait(bars.kv_empty(0), 1, abort_flag, a.err, kTimeoutNs);
+          if (!ok) break;
+          dev::mbar_arrive_expect_tx(bars.kv_full(0), kTileBytes);
+          load_kv_tile(sbase + kSmemKV, &tm_k, bars.kv_full(0), g.head, g.kv0 + g.lo * kTileRows, pol_kv);
+          grp = 1;
+        }
         for (int j = g.lo; ok && j < g.hi; ++j) {
-          const int32_t row = g.kv0 + j * kTileRows;
-          for (int t = 0; t < 2; ++t) {  // K then V
-            const uint32_t slot = kv_it % kSlots;
-            ok = dev::mbar_wait(bars.kv_empty(slot), ((kv_it / kSlots) & 1) ^ 1, abort_flag, a.err,
-                                        kTimeoutNs);
-            if (!ok) break;
-            const uint32_t dst = sbase + kSmemKV + slot * kTileBytes;
-            const CUtensorMap* tm = t == 0 ? &tm_k : &tm_v;
-            dev::mbar_arrive_expect_tx(bars.kv_full(slot), kTileBytes);
-            dev::tma_load_2d(dst, tm, bars.kv_full(slot), g.head * 128, row, pol_kv);
-            dev::tma_load_2d(dst + kHalfTileBytes, tm, bars.kv_full(slot), g.head * 128 + 64, row, pol_kv);
-            ++kv_it;
+          bool has_k = j + 1 < g.hi;
+          int k_head = g.head;
+          int32_t k_row = g.kv0 + (j + 1) * kTileRows;
+          if (!has_k && u + (int)gridDim.x < a.n_units) {
+            const UnitGeom n = unit_geom(a.units, u + gridDim.x);
+            has_k = true;
+            k_head = n.head;
+            k_row = n.kv0 + n.lo * kTileRows;
           }
+          const uint32_t b = grp & 1;
+          ok = dev::mbar_wait(bars.kv_empty(b), ((grp >> 1) & 1) ^ 1, abort_flag, a.err, kTimeoutNs);
+          if (!ok) break;
+          dev::mbar_arrive_expect_tx(bars.kv_full(b), has_k ? 2 * kTileBytes : kTileBytes);
+          load_kv_tile(sbase + kSmemKV + ((2 * grp - 1) % kSlots) * kTileBytes, &tm_v, bars.kv_full(b), g.head,
+                       g.kv0 + j * kTileRows, pol_kv);
+          if (has_k)
+            load_kv_tile(sbase + kSmemKV + ((2 * grp) % kSlots) * kTileBytes, &tm_k, bars.kv_full(b), k_head, k_row,
+                         pol_kv);
+          ++grp;
         }
       }
       if (!ok) {
         // drain: wait (bounded) for every copy this thread issued into the ring and Q
-        for (uint32_t r = 0; r < kSlots && r < kv_it; ++r) {
-          const uint32_t it = kv_it - 1 - r;
-          dev::mbar_wait_bounded(bars.kv_full(it % kSlots), (it / kSlots) & 1, nullptr, nullptr, kTimeoutNs);
+        for (uint32_t r = 1; r <= 2 && r <= grp; ++r) {
+          const uint32_t n = grp - r;
+          dev::mbar_wait_bounded(bars.kv_full(n & 1), (n >> 1) & 1, nullptr, nullptr, kTimeoutNs);
         }
 #pragma unroll
         for (int s = 0; s < 2; ++s)
@@ -233,19 +259,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // -------------------------------------------------------- MMA issuer ----
     if (lane == 0) {
-      uint32_t kv_it = 0, q_it0 = 0, q_it1 = 0, p_it0 = 0, p_it1 = 0;
+      uint32_t grp = 0, q_it0 = 0, q_it1 = 0, p_it0 = 0, p_it1 = 0;
       bool ok = true;
       bool issued = false;
       for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
         const UnitGeom g = unit_geom(a.units, u);
+        const bool last_unit = u + (int)gridDim.x >= a.n_units;
         ok = dev::mbar_wait(bars.q_full(0), q_it0 & 1, abort_flag, a.err, kTimeoutNs);
         ++q_it0;
         if (ok && g.n_st > 1) {
           ok = dev::mbar_wait(bars.q_full(1), q_it1 & 1, abort_flag, a.err, kTimeoutNs);
           ++q_it1;
         }
-        const uint32_t k0 = kv_it % kSlots;
-        if (ok) ok = dev::mbar_wait(bars.kv_full(k0), (kv_it / kSlots) & 1, abort_flag, a.err, kTimeoutNs);
+        // this unit's first K tile: group 0 (first unit) or the K half of the
+        // previous unit's last group (already waited for)
+        uint32_t k0, rel;
+        if (u == (int)blockIdx.x) {
+          if (ok) ok = dev::mbar_wait(bars.kv_full(0), 0, abort_flag, a.err, kTimeoutNs);
+          k0 = 0;
+          rel = 0;
+          grp = 1;
+        } else {
+          k0 = (2 * (grp - 1)) % kSlots;
+          rel = grp - 1;
+        }
         if (!ok) break;
         dev::tc_fence_after();
 #pragma unroll
@@ -255,13 +292,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           dev::mma_commit(bars.s_ready(s));
           if (g.hi - g.lo == 1) dev::mma_commit(bars.q_empty(s));
         }
-        dev::mma_commit(bars.kv_empty(k0));
+        dev::mma_commit(bars.kv_empty(rel & 1));  // that K tile (and the V tile before it) are done
         issued = true;
         for (int j = g.lo; j < g.hi; ++j) {
-          const uint32_t it_v = kv_it + 1, it_k = kv_it + 2;
-          const uint32_t vslot = it_v % kSlots, kslot = it_k % kSlots;
+          const uint32_t b = grp & 1;
+          const uint32_t vslot = (2 * grp - 1) % kSlots, kslot = (2 * grp) % kSlots;
           const bool more = j + 1 < g.hi;
-          ok = dev::mbar_wait(bars.kv_full(vslot), (it_v / kSlots) & 1, abort_flag, a.err, kTimeoutNs);
+          ok = dev::mbar_wait(bars.kv_full(b), (grp >> 1) & 1, abort_flag, a.err, kTimeoutNs);
           if (!ok) break;
 #pragma unroll
           for (int s = 0; s < 2; ++s) {
@@ -273,12 +310,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             dev::tc_fence_after();
             issue_pv(tmem + 256 + s * 128, tmem + s * 128, sbase + kSmemKV + vslot * kTileBytes, j > g.lo);
             if (more) {
-              if (s == 0) {
-                ok = dev::mbar_wait(bars.kv_full(kslot), (it_k / kSlots) & 1, abort_flag, a.err,
-                                            kTimeoutNs);
-                if (!ok) break;
-                dev::tc_fence_after();
-              }
               issue_qk(tmem + s * 128, sbase + kSmemQ + s * kTileBytes, sbase + kSmemKV + kslot * kTileBytes);
               dev::mma_commit(bars.s_ready(s));
               if (j + 2 == g.hi) dev::mma_commit(bars.q_empty(s));
@@ -287,9 +318,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (!ok) break;
-          dev::mma_commit(bars.kv_empty(vslot));
-          if (more) dev::mma_commit(bars.kv_empty(kslot));
-          kv_it += 2;
+          // V(j) and K(j+1) are done; a unit's last group also holds the next
+          // unit's first K tile and is released after that QK (next prologue)
+          if (more || last_unit) dev::mma_commit(bars.kv_empty(b));
+          ++grp;
         }
       }
       if (!ok && issued) {
