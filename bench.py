@@ -198,6 +198,20 @@ def traffic_for_current_kernel():
     return int(rec["dram_bytes_per_launch"])
 
 
+def max_over_ranks(ms: float, device) -> float:
+    """The slowest rank's time (the job ends when its last replica does)."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world_size: int, flops_per_step: int, steps: int, ms: float) -> float:
+    """Whole-job throughput: every rank runs one replica's steps in ms."""
+    return world_size * flops_per_step * steps / (ms * 1e-3) / 1e12
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -271,9 +285,7 @@ def run_ours(args):
     fwd_ms = float(np.mean([ev[i][1].elapsed_time(ev[i][2]) for i in range(K)]))
     checksum = float(o.float().abs().sum().item())  # consume the output
     if ws > 1:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+        elapsed_ms = max_over_ranks(elapsed_ms, dev)
 
     # End to end through the public API with host buffers: every step copies
     # its q, k, v from pinned host memory to the device, runs the prologue and
@@ -328,14 +340,12 @@ def run_ours(args):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1)
     if ws > 1:
-        tt = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt.item())
+        e2e_ms = max_over_ranks(e2e_ms, dev)
     H.h3attn_get_device_error(plan.handle, stream=stream)
 
     pk = peaks()
     flops = w.flops()
-    value = ws * flops * K / (elapsed_ms * 1e-3) / 1e12
+    value = job_tflops(ws, flops, K, elapsed_ms)
     fwd_tflops = flops / (fwd_ms * 1e-3) / 1e12
     elem_bytes = S * W * 2
     pro_bytes = 4 * elem_bytes + S * 48 * 8  # q, k read + written, rope table
@@ -366,7 +376,7 @@ def run_ours(args):
             "prologue": {"bound": "hbm", "achieved": pro_gbs, "peak": pk["hbm_gbs"], "unit": "GB/s",
                          "frac": pro_gbs / pk["hbm_gbs"], "algorithmic_bytes": pro_bytes},
             "cpu_baseline": cpu,
-            "e2e": {"value": ws * flops * K2 / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+            "e2e": {"value": job_tflops(ws, flops, K2, e2e_ms), "unit": UNIT,
                     "h2d_bytes_per_step": 3 * elem_bytes, "d2h_bytes_per_step": elem_bytes,
                     "ms_per_step": e2e_ms / K2,
                     "method": "pinned host buffers; H2D of q, k, v and D2H of o every step on copy "
