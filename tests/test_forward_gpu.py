@@ -134,3 +134,17 @@ def test_forward_rejects_bad_arguments(lib):
             H.h3attn_forward(p.handle, q, k, v, o, 0.1, qkv_row_stride=100, o_row_stride=256)
         H.h3attn_forward(p.handle, q, k, v, o, 0.1)  # valid call still works
         H.h3attn_get_device_error(p.handle)
+
+
+def test_shipped_dit_geometry_fused_qkv(lib):
+    # the shipped DiT block: 56 heads x 128 (hidden 7168), q/k/v read straight
+    # out of a fused-qkv buffer [S, 3*H*128] through the row stride, prologue in place
+    lens = [1000, 777]
+    docs = docs_1d(lens)
+    Hh = 56
+    t = random_tensors(sum(lens), Hh, seed=56)
+    r = run_product(docs, Hh, t, fused=True)
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    rows = sample_rows(cu, per_edge=24, interior=24, seed=56)
+    _, o, lse, _ = oracle_reference(docs, t, rows=rows)
+    check_attention(r.o[rows], o, r.lse[:, rows], lse, "56 heads, fused qkv, end to end")
