@@ -166,8 +166,8 @@ h3attn_status h3attn_forward(h3attn_plan_t plan, const void* q, const void* k, c
  * the work list is built on the host and, with the kernel's error word, kept
  * in one static device array of 1 MiB + 16 B that every GPU loading the
  * library holds until the process exits.  At most 32768 work units (a unit is
- * up to 256 query rows of one head in one document, so sum over documents of
- * ceil(len/256) * num_heads <= 32768); larger layouts get EINVAL with a
+ * up to 512 query rows of one head in one document, so sum over documents of
+ * ceil(len/512) * num_heads <= 32768); larger layouts get EINVAL with a
  * message.  q, k, v, o, lse_out and their rules are those of h3attn_forward,
  * except that o must not share any byte range with q, k or v.
  * Calls no cudaMalloc/cudaFree or other allocating routine.  The first call

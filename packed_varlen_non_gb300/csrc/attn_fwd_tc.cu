@@ -1,4 +1,5 @@
-// Packed varlen non-causal attention on the 5th-generation tensor cores.
+// Packed varlen non-causal attention on the 5th-generation tensor cores,
+// run by CTA pairs.
 //
 // Pages: vllm.cpp PR #26 "feat(minimax-h3)", PR description (packed varlen
 // NON-CAUSAL attention: each query attends to every key of its own
@@ -6,41 +7,61 @@
 // flash-attention call with causal=false) and the warp-per-query-row commit
 // (online-softmax recurrence in f32; Q read once per query row).
 //
-// Design (one persistent CTA per SM, 10 warps):
-//   warp 9       TMA producer: Q tiles of the work unit, then the unit's
-//                document's K and V tiles through a 4-slot shared-memory ring,
-//                V(j) and the next K tile loaded as one group behind one
-//                barrier (one readiness poll and one release per key tile).
-//   warp 8       MMA issuer (one thread) and TMEM owner: S_s = Q_s K_j^T and
-//                O_s += P_s V_j with tcgen05.mma, fp32 accumulators in TMEM.
-//   warps 0..3   softmax for query tile 0 (rows 0..127 of the unit),
-//   warps 4..7   softmax for query tile 1 (rows 128..255): one thread per
-//                query row reads its S row from TMEM, keeps the running max
-//                and sum in registers (no cross-thread reduction is needed
-//                since a thread owns a whole row), writes P as bf16 back into
-//                TMEM over its S columns, rescales its O row when the max has
-//                grown by more than 2^8, and at the end of the unit writes
-//                O / l and the log-sum-exp.
-// While one softmax group works on its tile, the tensor core runs the other
-// tile's MMAs (two-tile ping-pong).  A work unit (head, document, 256 query
-// rows) only visits its own document's key tiles; keys past the document end
-// in the last tile are masked to -inf, rows past it are never stored.
+// Design: a cluster of two CTAs (one per SM of a pair) works on one unit of
+// 512 query rows of one (head, document); each CTA owns 256 of them as two
+// 128-row query tiles s = 0, 1 (rows q0 + 256 s + 128 rank + i).  The MMAs are
+// pair instructions (tcgen05 cta_group::2, M = 256): one thread of the even
+// CTA issues them, each CTA's tensor core computes its own 128 rows, and each
+// CTA holds only half of every B operand -- keys [64 rank, 64 rank + 64) of a
+// K tile and dims [64 rank, 64 rank + 64) of a V tile -- so a CTA reads
+// (and loads from L2) half the key/value bytes a single-CTA kernel would.
+// Per CTA, 10 warps:
+//   warp 9       TMA producer: its own Q tiles, then its halves of the
+//                document's K and V tiles through an 8-slot ring; V(j) and the
+//                next K tile form one group behind one barrier.
+//   warp 8       even CTA: MMA issuer for the pair, S_s = Q_s K_j^T and
+//                O_s += P_s V_j, fp32 accumulators in TMEM; odd CTA: relays
+//                the arrival of its Q tiles to the even CTA's barriers.  Both
+//                allocate the pair's TMEM together.
+//   warps 0..3   softmax for query tile 0 of this CTA,
+//   warps 4..7   softmax for query tile 1: one thread per query row reads its
+//                S row from TMEM, keeps the running max and sum in registers,
+//                writes P as bf16 back into TMEM over its S columns, rescales
+//                its O row when the max has grown by more than 2^8, and at the
+//                end of the unit writes O / l and the log-sum-exp.
+// While one softmax group works on its tile, the tensor cores run the other
+// tile's MMAs (two-tile ping-pong).  A unit only visits its own document's key
+// tiles; keys past the document end in the last tile are masked to -inf, rows
+// past it are never stored.
 //
-// TMEM columns: S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512); P_s is
-// bf16 packed two per column in the first 64 columns of S_s.
+// TMEM columns (each CTA): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512);
+// P_s is bf16 packed two per column in the first 64 columns of S_s.
 //
-// Shared memory tiles are 128 rows x 64 bf16 (128 B per row, 128-byte TMA
-// swizzle); a 128 x 128 tile is two of them 16 KB apart.  Q and K are K-major
-// operands; V is the MN-major B operand of the PV product.
+// Shared memory rows are 64 bf16 (128 B, 128-byte TMA swizzle).  Q tiles are
+// 128 rows x 128 dims (two 16 KB halves); a K half-tile is 64 keys x 128 dims
+// (two 8 KB halves), a V half-tile 128 keys x 64 dims (16 KB).  Q and K are
+// K-major operands; V is the MN-major B operand of the PV product.
 //
-// Every mbarrier wait is bounded (mbar_wait_bounded): on expiry the CTA
-// raises an abort flag, records a timeout in the device error word, drains
-// its own copies and MMAs with bounded waits, frees TMEM and exits.
+// Barriers: completion of the pair's MMAs is multicast to both CTAs (S ready,
+// O ready, Q slots free).  The MMA-issuing thread paces the tensor cores, so
+// per key tile it only waits for P and commits S: its "P ready" barrier
+// counts one arrival per softmax warp of both CTAs, and softmax warp 0 of
+// each CTA arrives only once its CTA's next K/V group has landed; a softmax
+// thread that sees S of key tile t ready frees the ring slots of the group
+// holding K(t) (everything before that QK has completed).  Q tiles: the even
+// CTA's "full" barrier expects one more arrival, made by the odd CTA's relay
+// once the odd CTA's tile has landed.
+//
+// Every mbarrier wait is bounded: on expiry the CTA raises an abort flag,
+// records a timeout in the device error word, drains its own copies and MMAs
+// with bounded waits, and leaves through the cluster barrier, where the pair
+// frees its TMEM together.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <cstdio>
 
 #include "device_common.cuh"
 
@@ -52,24 +73,29 @@ constexpr int kThreads = 320;
 constexpr int kMmaWarp = 8;
 constexpr int kTmaWarp = 9;
 constexpr int kTileRows = 128;
-constexpr int kSlots = 4;
-constexpr uint32_t kHalfTileBytes = 128 * 128;        // 128 rows x 128 B
-constexpr uint32_t kTileBytes = 2 * kHalfTileBytes;   // 32 KB
-constexpr uint32_t kSmemQ = 0;                        // 2 tiles
-constexpr uint32_t kSmemKV = 2 * kTileBytes;          // kSlots tiles
-constexpr uint32_t kSmemBar = kSmemKV + kSlots * kTileBytes;
-// barriers: q_full[2] q_empty[2] kv_full[4] kv_empty[4] s_ready[2] p_ready[2] o_ready[2] drain
-constexpr int kNumBars = 2 + 2 + kSlots + kSlots + 2 + 2 + 2 + 1;
+constexpr int kSlots = 8;                              // ring slots (16 KB each)
+constexpr int kGroups = kSlots / 2;                    // key/value groups in flight
+constexpr uint32_t kQTileBytes = 128 * 128 * 2;        // 32 KB, two 16 KB halves
+constexpr uint32_t kQHalfBytes = kQTileBytes / 2;
+constexpr uint32_t kSlotBytes = 64 * 128 * 2;          // 16 KB
+constexpr uint32_t kKHalfBytes = kSlotBytes / 2;       // 64 keys x 64 dims
+constexpr uint32_t kSmemQ = 0;                         // 2 tiles
+constexpr uint32_t kSmemKV = 2 * kQTileBytes;          // kSlots slots
+constexpr uint32_t kSmemBar = kSmemKV + kSlots * kSlotBytes;
+// barriers: q_full[2] q_empty[2] kv_full[G] kv_empty[G] s_ready[2] p_ready[2] o_ready[2] drain
+constexpr int kNumBars = 2 + 2 + kGroups + kGroups + 2 + 2 + 2 + 1;
 constexpr uint32_t kSmemMisc = kSmemBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kSmemMisc + 16;
-constexpr size_t kSmemAlloc = kSmemBytes + 1024;      // slack to align the base to 1 KB
+constexpr size_t kSmemAlloc = kSmemBytes + 1024;       // slack to align the base to 1 KB
 constexpr uint32_t kTmemCols = 512;
-constexpr uint64_t kTimeoutNs = 2000000000ull;        // 2 s
-constexpr float kRescaleThreshold = 8.0f;             // log2 units: rescale when max grows by > 2^8
+constexpr uint64_t kTimeoutNs = 2000000000ull;         // 2 s
+constexpr float kRescaleThreshold = 8.0f;              // log2 units: rescale when max grows by > 2^8
+constexpr uint16_t kPairMask = 0x3;
+static_assert(kUnitRows == 4 * kTileRows, "a unit is two query tiles in each CTA of the pair");
 
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, M = 128, N = 128.
-constexpr uint32_t kIdescBase = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((128u >> 4) << 24);
-constexpr uint32_t kIdescQK = kIdescBase;             // A, B K-major
+// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, M = 256 (pair), N = 128.
+constexpr uint32_t kIdescBase = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((256u >> 4) << 24);
+constexpr uint32_t kIdescQK = kIdescBase;              // A, B K-major
 constexpr uint32_t kIdescPV = kIdescBase | (1u << 16);  // B (V) MN-major
 
 // Shared-memory matrix descriptor with 128-byte swizzling.
@@ -83,11 +109,11 @@ struct Bars {
   __device__ uint32_t q_full(int s) const { return base + 8 * s; }
   __device__ uint32_t q_empty(int s) const { return base + 8 * (2 + s); }
   __device__ uint32_t kv_full(int i) const { return base + 8 * (4 + i); }
-  __device__ uint32_t kv_empty(int i) const { return base + 8 * (4 + kSlots + i); }
-  __device__ uint32_t s_ready(int s) const { return base + 8 * (4 + 2 * kSlots + s); }
-  __device__ uint32_t p_ready(int s) const { return base + 8 * (6 + 2 * kSlots + s); }
-  __device__ uint32_t o_ready(int s) const { return base + 8 * (8 + 2 * kSlots + s); }
-  __device__ uint32_t drain() const { return base + 8 * (10 + 2 * kSlots); }
+  __device__ uint32_t kv_empty(int i) const { return base + 8 * (4 + kGroups + i); }
+  __device__ uint32_t s_ready(int s) const { return base + 8 * (4 + 2 * kGroups + s); }
+  __device__ uint32_t p_ready(int s) const { return base + 8 * (6 + 2 * kGroups + s); }
+  __device__ uint32_t o_ready(int s) const { return base + 8 * (8 + 2 * kGroups + s); }
+  __device__ uint32_t drain() const { return base + 8 * (10 + 2 * kGroups); }
 };
 
 struct UnitGeom {
@@ -105,33 +131,43 @@ __device__ __forceinline__ UnitGeom unit_geom(const WorkUnit* units, int u) {
   g.lo = x.x;
   g.hi = x.y;
   g.part = x.z;
-  g.n_st = (w.x + kTileRows < w.z) ? 2 : 1;
+  g.n_st = (w.x + 2 * kTileRows < w.z) ? 2 : 1;  // query tile 1 of the pair holds rows from 256 on
   return g;
 }
 
-// One 128-row tile of K or V (two 64-column boxes) into a ring slot.
-__device__ __forceinline__ void load_kv_tile(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int head,
-                                             int32_t row, uint64_t pol) {
+// This CTA's half of a K tile: keys [key0 + 64 rank, +64), all 128 dims (two boxes).
+__device__ __forceinline__ void load_k_half(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int head,
+                                            int32_t key0, uint32_t rank, uint64_t pol) {
+  const int32_t row = key0 + 64 * (int32_t)rank;
   dev::tma_load_2d(dst, tm, bar, head * 128, row, pol);
-  dev::tma_load_2d(dst + kHalfTileBytes, tm, bar, head * 128 + 64, row, pol);
+  dev::tma_load_2d(dst + kKHalfBytes, tm, bar, head * 128 + 64, row, pol);
 }
 
-// S (TMEM, 128 x 128 fp32) = Q (smem, K-major) * K^T (smem, K-major), 8 MMAs of K = 16.
+// This CTA's half of a V tile: 128 keys, dims [64 rank, 64 rank + 64) (one box).
+__device__ __forceinline__ void load_v_half(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int head,
+                                            int32_t key0, uint32_t rank, uint64_t pol) {
+  dev::tma_load_2d(dst, tm, bar, head * 128 + 64 * (int32_t)rank, key0, pol);
+}
+
+// S (TMEM, 128 x 128 fp32 in each CTA) = Q (smem, K-major) * K^T (smem, K-major,
+// 64 keys per CTA), 8 pair MMAs of K = 16.
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk) {
-    const uint32_t off = (kk >> 2) * kHalfTileBytes + (kk & 3) * 32;
-    dev::mma_ss(d_tmem, smem_desc(q_smem + off, 16, 1024), smem_desc(k_smem + off, 16, 1024), kIdescQK,
-                kk > 0 ? 1u : 0u);
+    const uint32_t qo = (kk >> 2) * kQHalfBytes + (kk & 3) * 32;
+    const uint32_t ko = (kk >> 2) * kKHalfBytes + (kk & 3) * 32;
+    dev::mma_ss_pair(d_tmem, smem_desc(q_smem + qo, 16, 1024), smem_desc(k_smem + ko, 16, 1024), kIdescQK,
+                     kk > 0 ? 1u : 0u);
   }
 }
 
-// O (TMEM fp32) (+)= P (TMEM, bf16 pairs) * V (smem, MN-major), 8 MMAs of K = 16 keys.
+// O (TMEM fp32) (+)= P (TMEM, bf16 pairs) * V (smem, MN-major, 64 dims per CTA),
+// 8 pair MMAs of K = 16 keys.
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, bool acc) {
 #pragma unroll
   for (int kk = 0; kk < 8; ++kk)
-    dev::mma_ts(d_tmem, p_tmem + kk * 8, smem_desc(v_smem + kk * 16 * 128, kHalfTileBytes, 1024), kIdescPV,
-                (acc || kk > 0) ? 1u : 0u);
+    dev::mma_ts_pair(d_tmem, p_tmem + kk * 8, smem_desc(v_smem + kk * 16 * 128, kSlotBytes, 1024), kIdescPV,
+                     (acc || kk > 0) ? 1u : 0u);
 }
 
 // One query row's 128 scores from TMEM (4 loads of 32 columns); keys past
@@ -147,7 +183,7 @@ __device__ __forceinline__ void load_scores(uint32_t t_s, uint32_t (&r)[4][32], 
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, ForwardArgs a) {
   extern __shared__ unsigned char smem_raw[];
@@ -160,17 +196,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t warp = dev::warp_id_uniform();
   const uint32_t lane = threadIdx.x & 31;
+  const uint32_t rank = dev::cluster_ctarank();   // 0: issues the pair's MMAs
+  const int pair = (int)(blockIdx.x >> 1), n_pairs = (int)(gridDim.x >> 1);
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     for (int s = 0; s < 2; ++s) {
-      dev::mbar_init(bars.q_full(s), 1);
+      dev::mbar_init(bars.q_full(s), rank == 0 ? 2 : 1);  // even CTA: own copies + the odd CTA's relay
       dev::mbar_init(bars.q_empty(s), 1);
       dev::mbar_init(bars.s_ready(s), 1);
-      dev::mbar_init(bars.p_ready(s), kTileRows);
+      dev::mbar_init(bars.p_ready(s), 8);           // one arrival per softmax warp of the pair
       dev::mbar_init(bars.o_ready(s), 1);
     }
-    for (int i = 0; i < kSlots; ++i) {
+    for (int i = 0; i < kGroups; ++i) {
       dev::mbar_init(bars.kv_full(i), 1);
       dev::mbar_init(bars.kv_empty(i), 1);
     }
@@ -183,11 +221,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     dev::tma_prefetch_desc(&tm_v);
   }
   if (warp == kMmaWarp) {
-    dev::tmem_alloc(dev::smem_u32(tmem_slot), kTmemCols);
-    dev::tmem_relinquish();
+    dev::tmem_alloc_pair(dev::smem_u32(tmem_slot), kTmemCols);
+    dev::tmem_relinquish_pair();
   }
   dev::tc_fence_before();
   __syncthreads();
+  __syncwarp();
+  dev::cluster_sync();  // both CTAs' barriers are initialised before any cross-CTA arrival
   dev::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -198,108 +238,126 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t pol_kv = dev::policy_evict_last();
       uint32_t grp = 0, q_it[2] = {0, 0};
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+      for (int u = pair; ok && u < a.n_units; u += n_pairs) {
         const UnitGeom g = unit_geom(a.units, u);
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
           if (!ok || s >= g.n_st) break;
           ok = dev::mbar_wait(bars.q_empty(s), (q_it[s] & 1) ^ 1, abort_flag, a.err, kTimeoutNs);
           if (!ok) break;
-          const uint32_t dst = sbase + kSmemQ + s * kTileBytes;
-          dev::mbar_arrive_expect_tx(bars.q_full(s), kTileBytes);
-          const int32_t row = g.q0 + s * kTileRows;
+          const uint32_t dst = sbase + kSmemQ + s * kQTileBytes;
+          dev::mbar_arrive_expect_tx(bars.q_full(s), kQTileBytes);
+          const int32_t row = g.q0 + s * 2 * kTileRows + (int32_t)rank * kTileRows;
           dev::tma_load_2d(dst, &tm_q, bars.q_full(s), g.head * 128, row, pol_q);
-          dev::tma_load_2d(dst + kHalfTileBytes, &tm_q, bars.q_full(s), g.head * 128 + 64, row, pol_q);
+          dev::tma_load_2d(dst + kQHalfBytes, &tm_q, bars.q_full(s), g.head * 128 + 64, row, pol_q);
           ++q_it[s];
         }
         // Key/value groups: group 0 is the first unit's first K tile (ring slot
         // 0); group n >= 1 is V(j) with the next K tile -- K(j+1), or the next
-        // unit's first K tile -- in slots (2n-1) % 4 and 2n % 4, one full and
-        // one empty barrier (index n & 1) for both.
-        if (u == (int)blockIdx.x) {
+        // unit's first K tile -- in slots (2n-1) % kSlots and 2n % kSlots, one
+        // full and one empty barrier (index n % kGroups) for both.
+        if (u == pair) {
           ok = dev::mbar_wait(bars.kv_empty(0), 1, abort_flag, a.err, kTimeoutNs);
           if (!ok) break;
-          dev::mbar_arrive_expect_tx(bars.kv_full(0), kTileBytes);
-          load_kv_tile(sbase + kSmemKV, &tm_k, bars.kv_full(0), g.head, g.kv0 + g.lo * kTileRows, pol_kv);
+          dev::mbar_arrive_expect_tx(bars.kv_full(0), kSlotBytes);
+          load_k_half(sbase + kSmemKV, &tm_k, bars.kv_full(0), g.head, g.kv0 + g.lo * kTileRows, rank, pol_kv);
           grp = 1;
         }
         for (int j = g.lo; ok && j < g.hi; ++j) {
           bool has_k = j + 1 < g.hi;
           int k_head = g.head;
           int32_t k_row = g.kv0 + (j + 1) * kTileRows;
-          if (!has_k && u + (int)gridDim.x < a.n_units) {
-            const UnitGeom n = unit_geom(a.units, u + gridDim.x);
+          if (!has_k && u + n_pairs < a.n_units) {
+            const UnitGeom n = unit_geom(a.units, u + n_pairs);
             has_k = true;
             k_head = n.head;
             k_row = n.kv0 + n.lo * kTileRows;
           }
-          const uint32_t b = grp & 1;
-          ok = dev::mbar_wait(bars.kv_empty(b), ((grp >> 1) & 1) ^ 1, abort_flag, a.err, kTimeoutNs);
+          const uint32_t b = grp % kGroups;
+          ok = dev::mbar_wait(bars.kv_empty(b), ((grp / kGroups) & 1) ^ 1, abort_flag, a.err, kTimeoutNs);
           if (!ok) break;
-          dev::mbar_arrive_expect_tx(bars.kv_full(b), has_k ? 2 * kTileBytes : kTileBytes);
-          load_kv_tile(sbase + kSmemKV + ((2 * grp - 1) % kSlots) * kTileBytes, &tm_v, bars.kv_full(b), g.head,
-                       g.kv0 + j * kTileRows, pol_kv);
+          dev::mbar_arrive_expect_tx(bars.kv_full(b), has_k ? 2 * kSlotBytes : kSlotBytes);
+          load_v_half(sbase + kSmemKV + ((2 * grp - 1) % kSlots) * kSlotBytes, &tm_v, bars.kv_full(b), g.head,
+                      g.kv0 + j * kTileRows, rank, pol_kv);
           if (has_k)
-            load_kv_tile(sbase + kSmemKV + ((2 * grp) % kSlots) * kTileBytes, &tm_k, bars.kv_full(b), k_head, k_row,
-                         pol_kv);
+            load_k_half(sbase + kSmemKV + ((2 * grp) % kSlots) * kSlotBytes, &tm_k, bars.kv_full(b), k_head,
+                        k_row, rank, pol_kv);
           ++grp;
         }
       }
       if (!ok) {
         // drain: wait (bounded) for every copy this thread issued into the ring and Q
-        for (uint32_t r = 1; r <= 2 && r <= grp; ++r) {
+        // (the even CTA's Q barriers also need the relay's arrival: a wait
+        // that times out here only delays the exit)
+        for (uint32_t r = 1; r <= (uint32_t)kGroups && r <= grp; ++r) {
           const uint32_t n = grp - r;
-          dev::mbar_wait_bounded(bars.kv_full(n & 1), (n >> 1) & 1, nullptr, nullptr, kTimeoutNs);
+          dev::mbar_wait_bounded(bars.kv_full(n % kGroups), (n / kGroups) & 1, nullptr, nullptr, kTimeoutNs);
         }
 #pragma unroll
         for (int s = 0; s < 2; ++s)
-          if (q_it[s]) dev::mbar_wait_bounded(bars.q_full(s), (q_it[s] - 1) & 1, nullptr, nullptr, kTimeoutNs);
+          if (q_it[s])
+            dev::mbar_wait_bounded(bars.q_full(s), (q_it[s] - 1) & 1, nullptr, nullptr, kTimeoutNs);
+      }
+    }
+  } else if (warp == kMmaWarp && rank != 0) {
+    // ------------------------------------------- relay (odd CTA of the pair) ----
+    // As each of this CTA's Q tiles lands (and, before the first, the first K
+    // group), arrives on the even CTA's matching barrier.
+    if (lane == 0) {
+      uint32_t q_it[2] = {0, 0};
+      bool ok = dev::mbar_wait(bars.kv_full(0), 0, abort_flag, a.err, kTimeoutNs);
+      for (int u = pair; ok && u < a.n_units; u += n_pairs) {
+        const UnitGeom g = unit_geom(a.units, u);
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          if (!ok || s >= g.n_st) break;
+          ok = dev::mbar_wait(bars.q_full(s), q_it[s] & 1, abort_flag, a.err, kTimeoutNs);
+          if (!ok) break;
+          ++q_it[s];
+          dev::mbar_arrive_cluster(dev::mapa_shared(bars.q_full(s), 0));
+        }
       }
     }
   } else if (warp == kMmaWarp) {
-    // -------------------------------------------------------- MMA issuer ----
+    // ----------------------------------------- MMA issuer (even CTA, pair) ----
     if (lane == 0) {
       uint32_t grp = 0, q_it0 = 0, q_it1 = 0, p_it0 = 0, p_it1 = 0;
       bool ok = true;
       bool issued = false;
-      for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+      for (int u = pair; ok && u < a.n_units; u += n_pairs) {
         const UnitGeom g = unit_geom(a.units, u);
-        const bool last_unit = u + (int)gridDim.x >= a.n_units;
         ok = dev::mbar_wait(bars.q_full(0), q_it0 & 1, abort_flag, a.err, kTimeoutNs);
         ++q_it0;
         if (ok && g.n_st > 1) {
           ok = dev::mbar_wait(bars.q_full(1), q_it1 & 1, abort_flag, a.err, kTimeoutNs);
           ++q_it1;
         }
-        // this unit's first K tile: group 0 (first unit) or the K half of the
-        // previous unit's last group (already waited for)
-        uint32_t k0, rel;
-        if (u == (int)blockIdx.x) {
+        // this unit's first K tile: group 0 (first unit; the odd CTA's half is
+        // covered by its relay's Q arrival) or the K half of the previous
+        // unit's last group (covered by that unit's last P-ready barrier)
+        uint32_t k0;
+        if (u == pair) {
           if (ok) ok = dev::mbar_wait(bars.kv_full(0), 0, abort_flag, a.err, kTimeoutNs);
           k0 = 0;
-          rel = 0;
           grp = 1;
         } else {
           k0 = (2 * (grp - 1)) % kSlots;
-          rel = grp - 1;
         }
         if (!ok) break;
         dev::tc_fence_after();
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
           if (s >= g.n_st) break;
-          issue_qk(tmem + s * 128, sbase + kSmemQ + s * kTileBytes, sbase + kSmemKV + k0 * kTileBytes);
-          dev::mma_commit(bars.s_ready(s));
-          if (g.hi - g.lo == 1) dev::mma_commit(bars.q_empty(s));
+          issue_qk(tmem + s * 128, sbase + kSmemQ + s * kQTileBytes, sbase + kSmemKV + k0 * kSlotBytes);
+          dev::mma_commit_pair_mc(bars.s_ready(s), kPairMask);
+          if (g.hi - g.lo == 1) dev::mma_commit_pair_mc(bars.q_empty(s), kPairMask);
         }
-        dev::mma_commit(bars.kv_empty(rel & 1));  // that K tile (and the V tile before it) are done
         issued = true;
         for (int j = g.lo; j < g.hi; ++j) {
-          const uint32_t b = grp & 1;
+          // group grp = V(j) + the next K tile; its arrival in both CTAs is
+          // implied by P-ready of query tile 0
           const uint32_t vslot = (2 * grp - 1) % kSlots, kslot = (2 * grp) % kSlots;
           const bool more = j + 1 < g.hi;
-          ok = dev::mbar_wait(bars.kv_full(b), (grp >> 1) & 1, abort_flag, a.err, kTimeoutNs);
-          if (!ok) break;
 #pragma unroll
           for (int s = 0; s < 2; ++s) {
             if (s >= g.n_st) break;
@@ -308,25 +366,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             ++p_it;
             dev::tc_fence_after();
-            issue_pv(tmem + 256 + s * 128, tmem + s * 128, sbase + kSmemKV + vslot * kTileBytes, j > g.lo);
+            issue_pv(tmem + 256 + s * 128, tmem + s * 128, sbase + kSmemKV + vslot * kSlotBytes, j > g.lo);
             if (more) {
-              issue_qk(tmem + s * 128, sbase + kSmemQ + s * kTileBytes, sbase + kSmemKV + kslot * kTileBytes);
-              dev::mma_commit(bars.s_ready(s));
-              if (j + 2 == g.hi) dev::mma_commit(bars.q_empty(s));
+              issue_qk(tmem + s * 128, sbase + kSmemQ + s * kQTileBytes, sbase + kSmemKV + kslot * kSlotBytes);
+              dev::mma_commit_pair_mc(bars.s_ready(s), kPairMask);
+              if (j + 2 == g.hi) dev::mma_commit_pair_mc(bars.q_empty(s), kPairMask);
             } else {
-              dev::mma_commit(bars.o_ready(s));
+              dev::mma_commit_pair_mc(bars.o_ready(s), kPairMask);
             }
           }
           if (!ok) break;
-          // V(j) and K(j+1) are done; a unit's last group also holds the next
-          // unit's first K tile and is released after that QK (next prologue)
-          if (more || last_unit) dev::mma_commit(bars.kv_empty(b));
           ++grp;
         }
       }
       if (!ok && issued) {
         // drain: every MMA issued so far must finish before TMEM is freed
-        dev::mma_commit(bars.drain());
+        dev::mma_commit_pair(bars.drain());
         dev::mbar_wait_bounded(bars.drain(), 0, nullptr, nullptr, kTimeoutNs);
       }
     }
@@ -337,18 +392,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (warp & 3) * 32;
     const uint32_t t_s = tmem + (lane_base << 16) + st * 128;        // S_s / P_s
     const uint32_t t_o = tmem + (lane_base << 16) + 256 + st * 128;  // O_s
+    const uint32_t p_ready_remote = dev::mapa_shared(bars.p_ready(st), 0);
     uint32_t s_it = 0, o_it = 0;
+    uint32_t t0 = 0;                     // key tiles the pair has started before this unit
     bool ok = true;
     const float sl2 = a.scale_log2;
     __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.o);
-    for (int u = blockIdx.x; ok && u < a.n_units; u += gridDim.x) {
+    for (int u = pair; ok && u < a.n_units; u += n_pairs) {
       const UnitGeom g = unit_geom(a.units, u);
+      const uint32_t t_unit = t0;
+      t0 += g.hi - g.lo;
       if (st >= g.n_st) continue;
+      // ring bookkeeping by one lane of one warp per CTA
+      const bool releases = (warp & 3) == 0 && lane == 0 && st == g.n_st - 1;
+      const bool checks_kv = (warp & 3) == 0 && lane == 0 && st == 0;
       float m_used = -INFINITY, l = 0.f;
       for (int j = g.lo; j < g.hi; ++j) {
+        const uint32_t t = t_unit + (j - g.lo);  // the pair's running key-tile count
         ok = dev::mbar_wait(bars.s_ready(st), s_it & 1, abort_flag, a.err, kTimeoutNs);
         if (!ok) break;
         ++s_it;
+        // S of the last query tile is ready: every MMA before it is done, so
+        // the group holding K(t) (and V(t-1)) is free in this CTA
+        if (releases) dev::mbar_arrive(bars.kv_empty(t % kGroups));
         __syncwarp();  // lanes leave the wait separately; the TMEM loads are warp-collective
         dev::tc_fence_after();
         uint32_t r[4][32];
@@ -407,7 +473,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         dev::tmem_wait_st();
         dev::tc_fence_before();
-        dev::mbar_arrive(bars.p_ready(st));
+        __syncwarp();
+        // the next PV reads V(t) and the QK after it K(t+1): group t+1 must have
+        // landed in this CTA before query tile 0 reports P ready
+        if (checks_kv)
+          ok = dev::mbar_wait(bars.kv_full((t + 1) % kGroups), ((t + 1) / kGroups) & 1, abort_flag, a.err,
+                              kTimeoutNs);
+        if (lane == 0) dev::mbar_arrive_cluster(p_ready_remote);  // P (and O) of the warp's 32 rows
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
       }
       if (!ok) break;
       ok = dev::mbar_wait(bars.o_ready(st), o_it & 1, abort_flag, a.err, kTimeoutNs);
@@ -415,12 +491,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++o_it;
       __syncwarp();
       dev::tc_fence_after();
-      const int32_t row = g.q0 + st * kTileRows + row_in_tile;
+      const int32_t local = st * 2 * kTileRows + (int32_t)rank * kTileRows + (int32_t)row_in_tile;
+      const int32_t row = g.q0 + local;
       const bool valid = row < g.kv1;
       if (g.part >= 0) {
         // A piece of a unit split along the keys: unnormalised O row, its
         // reference max (log2 units) and sum, for the merge pass.
-        const size_t slot = (size_t)g.part * kUnitRows + st * kTileRows + row_in_tile;
+        const size_t slot = (size_t)g.part * kUnitRows + local;
         float4* dst = reinterpret_cast<float4*>(a.part_o + slot * kHeadDim);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -461,12 +538,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
+  // Neither CTA leaves (or frees the pair's TMEM) while the other may still
+  // arrive on its barriers or run MMAs on its shared memory and TMEM.
   dev::tc_fence_before();
   __syncthreads();
+  __syncwarp();  // the cluster barrier is warp-collective (.aligned)
+  dev::cluster_sync();
   if (warp == kMmaWarp) {
-    __syncwarp();  // lane 0 comes from the issue loop; dealloc is warp-collective
     dev::tc_fence_after();
-    dev::tmem_dealloc(tmem, kTmemCols);
+    dev::tmem_dealloc_pair(tmem, kTmemCols);
   }
 }
 
@@ -517,7 +597,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-bool make_map(CUtensorMap* m, const void* base, int64_t S, int32_t H, int64_t stride, std::string* why) {
+bool make_map(CUtensorMap* m, const void* base, int64_t S, int32_t H, int64_t stride, uint32_t box_rows,
+              std::string* why) {
   auto fn = encode_fn();
   if (fn == nullptr) {
     if (why) *why = "cuTensorMapEncodeTiled is unavailable";
@@ -525,7 +606,7 @@ bool make_map(CUtensorMap* m, const void* base, int64_t S, int32_t H, int64_t st
   }
   cuuint64_t dims[2] = {(cuuint64_t)H * kHeadDim, (cuuint64_t)S};
   cuuint64_t strides[1] = {(cuuint64_t)stride * 2};
-  cuuint32_t box[2] = {64, kTileRows};
+  cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -539,11 +620,39 @@ bool make_map(CUtensorMap* m, const void* base, int64_t S, int32_t H, int64_t st
 
 }  // namespace
 
-cudaError_t launch_forward(const ForwardArgs& a, int num_sms, cudaStream_t stream, std::string* why) {
+int forward_slots(int device, int num_sms) {
+  // Concurrent CTA pairs: the occupancy of the pair cluster (one CTA per SM),
+  // asked once per device; half the SMs if the query fails.
+  static int slots[64];
+  static std::once_flag once[64];
+  if (device < 0 || device >= 64) return num_sms / 2 > 0 ? num_sms / 2 : 1;
+  std::call_once(once[device], [device, num_sms] {
+    int n = 0;
+    int prev = -1;
+    cudaGetDevice(&prev);
+    if (prev != device) cudaSetDevice(device);
+    if (cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) ==
+        cudaSuccess) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(2 * (num_sms / 2 > 0 ? num_sms / 2 : 1));
+      cfg.blockDim = dim3(kThreads);
+      cfg.dynamicSmemBytes = kSmemAlloc;
+      if (cudaOccupancyMaxActiveClusters(&n, attn_fwd_tc_kernel, &cfg) != cudaSuccess) n = 0;
+    }
+    cudaGetLastError();
+    if (prev != device && prev >= 0) cudaSetDevice(prev);
+    slots[device] = n > 0 ? n : (num_sms / 2 > 0 ? num_sms / 2 : 1);
+    fprintf(stderr, "[probe] max active clusters %d, slots %d\n", n, slots[device]);
+  });
+  return slots[device];
+}
+
+cudaError_t launch_forward(const ForwardArgs& a, int device, int num_sms, cudaStream_t stream, std::string* why) {
   if (a.n_units == 0) return cudaSuccess;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, a.q, a.S, a.H, a.qkv_stride, why) || !make_map(&mk, a.k, a.S, a.H, a.qkv_stride, why) ||
-      !make_map(&mv, a.v, a.S, a.H, a.qkv_stride, why))
+  if (!make_map(&mq, a.q, a.S, a.H, a.qkv_stride, kTileRows, why) ||
+      !make_map(&mk, a.k, a.S, a.H, a.qkv_stride, kTileRows / 2, why) ||
+      !make_map(&mv, a.v, a.S, a.H, a.qkv_stride, kTileRows, why))
     return cudaErrorInvalidValue;
   static std::once_flag once;
   static cudaError_t attr = cudaSuccess;
@@ -554,8 +663,9 @@ cudaError_t launch_forward(const ForwardArgs& a, int num_sms, cudaStream_t strea
     if (why) *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
     return attr;
   }
-  const int grid = a.n_units < num_sms ? a.n_units : num_sms;
-  attn_fwd_tc_kernel<<<grid, kThreads, kSmemAlloc, stream>>>(mq, mk, mv, a);
+  const int slots = forward_slots(device, num_sms);
+  const int pairs = a.n_units < slots ? a.n_units : slots;
+  attn_fwd_tc_kernel<<<2 * pairs, kThreads, kSmemAlloc, stream>>>(mq, mk, mv, a);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess || a.n_merges == 0) return e;
   const int64_t warps = (int64_t)a.n_merges * kUnitRows;

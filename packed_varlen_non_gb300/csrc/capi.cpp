@@ -153,9 +153,9 @@ h3attn_status h3attn_plan_create(const h3attn_doc* docs, int32_t n_docs,
     return fail(H3ATTN_EUNSUPPORTED, "device %d is sm_%d%d; this library is built for sm_103a",
                 dev, major, minor);
   }
-  // the work list is balanced for one persistent CTA per SM
+  // the work list is balanced for the forward's persistent CTA pairs
   try {
-    build_plan_host(docs, n_docs, *opts, p->num_sms, *p);
+    build_plan_host(docs, n_docs, *opts, forward_slots(p->device, p->num_sms), *p);
   } catch (const std::bad_alloc&) {
     delete p;
     return fail(H3ATTN_ENOMEM, "host allocation failed while building the plan");
@@ -326,7 +326,7 @@ h3attn_status h3attn_forward(h3attn_plan_t plan, const void* q, const void* k, c
                 softmax_scale * 1.4426950408889634f, plan->d_units, plan->n_units, plan->d_err,
                 plan->d_merges, (int32_t)plan->merges_host.size(), plan->d_part_o, plan->d_part_ml};
   std::string why;
-  e = launch_forward(a, plan->num_sms, static_cast<cudaStream_t>(cuda_stream), &why);
+  e = launch_forward(a, plan->device, plan->num_sms, static_cast<cudaStream_t>(cuda_stream), &why);
   if (e != cudaSuccess) {
     if (!why.empty()) return fail(H3ATTN_ECUDA, "forward: %s", why.c_str());
     return cuda_fail(e, "forward launch");

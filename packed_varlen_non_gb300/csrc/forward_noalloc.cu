@@ -27,7 +27,7 @@ namespace h3 {
 
 namespace {
 
-constexpr int32_t kNoAllocMaxUnits = 32768;  // work units of up to 256 query rows x one head
+constexpr int32_t kNoAllocMaxUnits = 32768;  // work units of up to kUnitRows query rows x one head
 constexpr int kMaxDevices = 64;
 
 // [0]: device error word (cleared before every launch); [1 ..]: work list
@@ -151,7 +151,7 @@ extern "C" h3attn_status h3attn_forward_noalloc(const int32_t* cu_seqlens, int32
                 softmax_scale * 1.4426950408889634f, reinterpret_cast<const WorkUnit*>(scratch + 1),
                 (int32_t)n_units, reinterpret_cast<uint32_t*>(scratch), nullptr, 0, nullptr, nullptr};
   std::string why;
-  e = launch_forward(a, sms, st, &why);
+  e = launch_forward(a, dev, sms, st, &why);
   if (e != cudaSuccess)
     return fail(H3ATTN_ECUDA, "forward: %s", why.empty() ? cudaGetErrorString(e) : why.c_str());
   return H3ATTN_OK;

@@ -16,7 +16,7 @@ constexpr int kHeadDim = 128;
 constexpr int kRopeDims = 96;
 constexpr int kRopeHalf = 48;       // NeoX pairs (j, j + 48), one angle per pair
 constexpr int kAxisFreqs = 16;      // angles per axis: 32 rotated dims per axis / 2
-constexpr int kUnitRows = 256;      // query rows per attention work unit (two 128-row tiles)
+constexpr int kUnitRows = 512;      // query rows per attention work unit (a CTA pair, two 128-row tiles each)
 
 // Device error word values (the word is cleared by h3attn_get_device_error).
 constexpr uint32_t kErrNone = 0;
@@ -53,9 +53,9 @@ struct MergeUnit {
 };
 static_assert(sizeof(MergeUnit) == 32, "MergeUnit is read as two 16-byte vectors");
 
-// Build the segment list for a grid of `grid` persistent CTAs: whole units in
+// Build the segment list for `grid` persistent CTA pairs: whole units in
 // round-robin rounds, then the last partial round's units split along their
-// key tiles so that every CTA gets one piece (plan.cpp).
+// key tiles so that every pair gets one piece (plan.cpp).
 void build_segments(const std::vector<WorkUnit>& units, int grid, std::vector<WorkUnit>& segs,
                     std::vector<MergeUnit>& merges, int32_t* n_parts);
 
@@ -80,8 +80,8 @@ struct Plan {
   WorkUnit* d_units = nullptr;
   int32_t n_units = 0;
   MergeUnit* d_merges = nullptr;
-  float* d_part_o = nullptr;         // [n_parts, 256, 128] unnormalised O
-  float2* d_part_ml = nullptr;       // [n_parts, 256] (running max in log2 units, sum)
+  float* d_part_o = nullptr;         // [n_parts, kUnitRows, 128] unnormalised O
+  float2* d_part_ml = nullptr;       // [n_parts, kUnitRows] (running max in log2 units, sum)
   uint32_t* d_err = nullptr;         // device error word
 };
 
@@ -131,7 +131,10 @@ struct ForwardArgs {
   float* part_o;
   float2* part_ml;
 };
-cudaError_t launch_forward(const ForwardArgs& a, int num_sms, cudaStream_t stream,
+// Work slots of the forward: CTA pairs that run at the same time on `device`
+// (the plan's segment list is balanced for this many).
+int forward_slots(int device, int num_sms);
+cudaError_t launch_forward(const ForwardArgs& a, int device, int num_sms, cudaStream_t stream,
                            std::string* why);
 
 cudaError_t launch_selftest_bounded_wait(uint64_t timeout_ns, uint32_t* d_flag,

@@ -113,16 +113,16 @@ std::string build_plan_host(const h3attn_doc* docs, int32_t n_docs, const h3attn
 // Cost of a unit in tile MMAs: key tiles x active query tiles.
 static int64_t unit_cost(const WorkUnit& u) {
   const int64_t tiles = u.tile_hi - u.tile_lo;
-  return tiles * ((u.q_row0 + 128 < u.kv_end) ? 2 : 1);
+  return tiles * ((u.q_row0 + kUnitRows / 2 < u.kv_end) ? 2 : 1);
 }
 
 void build_segments(const std::vector<WorkUnit>& units, int grid, std::vector<WorkUnit>& segs,
                     std::vector<MergeUnit>& merges, int32_t* n_parts) {
-  // A persistent CTA takes segments c, c + grid, c + 2 grid, ...  Whole units
+  // A persistent CTA pair takes segments c, c + grid, c + 2 grid, ...  Whole units
   // fill the first floor(U / grid) rounds in list order (so the CTAs running
   // at one moment share heads and documents, and their keys stay in L2).
   // The L < grid units left for the last round are split along their key
-  // tiles into pieces of about equal cost, one piece per CTA, so the last
+  // tiles into pieces of about equal cost, one piece per pair, so the last
   // round is as long as one piece instead of one whole unit.
   segs.clear();
   merges.clear();
