@@ -98,12 +98,6 @@ constexpr uint32_t kIdescBase = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3
 constexpr uint32_t kIdescQK = kIdescBase;              // A, B K-major
 constexpr uint32_t kIdescPV = kIdescBase | (1u << 16);  // B (V) MN-major
 
-// Shared-memory matrix descriptor with 128-byte swizzling.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
-}
-
 struct Bars {
   uint32_t base;
   __device__ uint32_t q_full(int s) const { return base + 8 * s; }
@@ -149,25 +143,72 @@ __device__ __forceinline__ void load_v_half(uint32_t dst, const CUtensorMap* tm,
   dev::tma_load_2d(dst, tm, bar, head * 128 + 64 * (int32_t)rank, key0, pol);
 }
 
-// S (TMEM, 128 x 128 fp32 in each CTA) = Q (smem, K-major) * K^T (smem, K-major,
-// 64 keys per CTA), 8 pair MMAs of K = 16.
-__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk) {
-    const uint32_t qo = (kk >> 2) * kQHalfBytes + (kk & 3) * 32;
-    const uint32_t ko = (kk >> 2) * kKHalfBytes + (kk & 3) * 32;
-    dev::mma_ss_pair(d_tmem, smem_desc(q_smem + qo, 16, 1024), smem_desc(k_smem + ko, 16, 1024), kIdescQK,
-                     kk > 0 ? 1u : 0u);
-  }
+// Shared-memory descriptors, split into 32-bit words: the high word (stride
+// 1024 B between 8-row groups, descriptor version 1, 128-byte swizzle) is the
+// same for every operand here; the low word holds the start address >> 4 and
+// the leading-byte offset >> 4, and stepping through an operand only adds to
+// the address field (addresses stay below 256 KB, so it never carries).
+constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t desc_lo(uint32_t addr, uint32_t lbo) {
+  return ((addr >> 4) & 0x3FFFu) | ((lbo >> 4) << 16);
 }
 
-// O (TMEM fp32) (+)= P (TMEM, bf16 pairs) * V (smem, MN-major, 64 dims per CTA),
-// 8 pair MMAs of K = 16 keys.
+// S (TMEM, 128 x 128 fp32 in each CTA) = Q (smem, K-major) * K^T (smem, K-major,
+// 64 keys per CTA): 8 pair MMAs of K = 16 in one block.  Step kk reads Q at
+// +(kk/4) 16 KB + (kk%4) 32 B and K at +(kk/4) 8 KB + (kk%4) 32 B.
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+  const uint32_t qa = desc_lo(q_smem, 16), kb = desc_lo(k_smem, 16);
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 a, b;\n\t.reg .b32 x, y;\n\t"
+      "setp.ne.u32 p0, %4, %4;\n\t"
+      "setp.eq.u32 p1, %4, %4;\n\t"
+      "mov.b64 a, {%1, %3};\n\tmov.b64 b, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %5, p0;\n\t"
+      "add.u32 x, %1, 2;\n\tadd.u32 y, %2, 2;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %5, p1;\n\t"
+      "add.u32 x, %1, 4;\n\tadd.u32 y, %2, 4;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %5, p1;\n\t"
+      "add.u32 x, %1, 6;\n\tadd.u32 y, %2, 6;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %5, p1;\n\t"
+      "add.u32 x, %1, 1024;\n\tadd.u32 y, %2, 512;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %5, p1;\n\t"
+      "add.u32 x, %1, 1026;\n\tadd.u32 y, %2, 514;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %5, p1;\n\t"
+      "add.u32 x, %1, 1028;\n\tadd.u32 y, %2, 516;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %5, p1;\n\t"
+      "add.u32 x, %1, 1030;\n\tadd.u32 y, %2, 518;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %5, p1;\n\t}" ::"r"(d_tmem),
+      "r"(qa), "r"(kb), "r"(kDescHi), "r"(0u), "r"(kIdescQK)
+      : "memory");
+}
+
+// O (TMEM fp32) (+)= P (TMEM, bf16 pairs) * V (smem, MN-major, 64 dims per CTA):
+// 8 pair MMAs of K = 16 keys in one block.  Step kk reads P at TMEM column
+// +8 kk and V at +2 KB kk; the first accumulates only if acc.
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, bool acc) {
-#pragma unroll
-  for (int kk = 0; kk < 8; ++kk)
-    dev::mma_ts_pair(d_tmem, p_tmem + kk * 8, smem_desc(v_smem + kk * 16 * 128, kSlotBytes, 1024), kIdescPV,
-                     (acc || kk > 0) ? 1u : 0u);
+  const uint32_t vb = desc_lo(v_smem, kSlotBytes);
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 b;\n\t.reg .b32 t, y;\n\t"
+      "setp.ne.u32 p0, %4, 0;\n\t"
+      "setp.eq.u32 p1, %4, %4;\n\t"
+      "mov.b64 b, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], b, %5, p0;\n\t"
+      "add.u32 t, %1, 8;\n\tadd.u32 y, %2, 128;\n\tmov.b64 b, {y, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [t], b, %5, p1;\n\t"
+      "add.u32 t, %1, 16;\n\tadd.u32 y, %2, 256;\n\tmov.b64 b, {y, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [t], b, %5, p1;\n\t"
+      "add.u32 t, %1, 24;\n\tadd.u32 y, %2, 384;\n\tmov.b64 b, {y, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [t], b, %5, p1;\n\t"
+      "add.u32 t, %1, 32;\n\tadd.u32 y, %2, 512;\n\tmov.b64 b, {y, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [t], b, %5, p1;\n\t"
+      "add.u32 t, %1, 40;\n\tadd.u32 y, %2, 640;\n\tmov.b64 b, {y, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [t], b, %5, p1;\n\t"
+      "add.u32 t, %1, 48;\n\tadd.u32 y, %2, 768;\n\tmov.b64 b, {y, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [t], b, %5, p1;\n\t"
+      "add.u32 t, %1, 56;\n\tadd.u32 y, %2, 896;\n\tmov.b64 b, {y, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [t], b, %5, p1;\n\t}" ::"r"(d_tmem),
+      "r"(p_tmem), "r"(vb), "r"(kDescHi), "r"(acc ? 1u : 0u), "r"(kIdescPV)
+      : "memory");
 }
 
 // One query row's 128 scores from TMEM (4 loads of 32 columns); keys past
