@@ -148,3 +148,47 @@ def test_shipped_dit_geometry_fused_qkv(lib):
     rows = sample_rows(cu, per_edge=24, interior=24, seed=56)
     _, o, lse, _ = oracle_reference(docs, t, rows=rows)
     check_attention(r.o[rows], o, r.lse[:, rows], lse, "56 heads, fused qkv, end to end")
+
+
+def _bf16_round(x):
+    """fp64 -> nearest-even bf16 values (as fp64), for crafted inputs."""
+    return synth.bf16_bits_to_f64(synth.f32_to_bf16_bits(np.asarray(x, dtype=np.float32)))
+
+
+@pytest.mark.parametrize("col", [20, 100])
+def test_running_max_jump_rescales_o(lib, col):
+    # Every query carries the same direction u; keys are small noise except one
+    # key per head in key tile 3 whose score is ~9.5 log2-units above the rest,
+    # so the running max grows by more than 2^8 in the middle of a unit (in the
+    # first or second half of the tile's columns) and O and l must be rescaled.
+    # About as much weight sits before the jump as after it.
+    L, Hh = 700, 2
+    rng = np.random.default_rng(col)
+    u = np.where(rng.random(128) < 0.5, -1.0, 1.0)
+    q = _bf16_round(u[None, None, :] + 0.2 * rng.standard_normal((L, Hh, 128)))
+    k = _bf16_round(0.05 * rng.standard_normal((L, Hh, 128)))
+    jump = 3 * 128 + col
+    k[jump, 0] = _bf16_round(0.58 * u)
+    k[jump, 1] = _bf16_round(0.58 * u)
+    v = _bf16_round(rng.standard_normal((L, Hh, 128)))
+    scale = 1.0 / np.sqrt(128.0)
+    dev = torch.device("cuda")
+    to_dev = lambda x: torch.from_numpy(x.reshape(L, Hh * 128)).to(dev).to(torch.bfloat16)
+    qd, kd, vd = to_dev(q), to_dev(k), to_dev(v)
+    o = torch.full((L, Hh * 128), float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full((Hh, L), float("nan"), dtype=torch.float32, device=dev)
+    with H.Plan(docs_1d([L]), Hh) as plan:
+        H.h3attn_forward(plan.handle, qd, kd, vd, o, scale, lse)
+        H.h3attn_get_device_error(plan.handle)
+    o_gpu = o.double().cpu().numpy().reshape(L, Hh, 128)
+    from oracle import attention as oatt
+    o_ref, lse_ref = oatt.attention_rows(q, k, v, np.array([0, L]), scale, range(Hh), np.arange(L))
+    # the inputs do what the test needs: the jump clears 2^8 for every row, and
+    # the weight is split between the keys before it and the jump key
+    s2 = np.einsum("ihd,jhd->hij", q, k) * scale / np.log(2.0)
+    others = np.delete(s2, jump, axis=2)
+    assert (s2[:, :, jump] - others.max(axis=2)).min() > 8.5
+    w = np.exp2(s2 - s2.max(axis=2, keepdims=True))
+    share = w[:, :, jump] / w.sum(axis=2)
+    assert 0.2 < share.min() and share.max() < 0.8
+    check_attention(o_gpu, o_ref, lse.cpu().numpy(), lse_ref, f"running max jump at column {col}")
