@@ -129,8 +129,12 @@ h3attn_status h3attn_plan_copy_rope_table(h3attn_plan_t plan, float* host_out);
  * out_row_stride (in place is allowed when the pointers and strides are
  * equal; partial overlap is not).  gain_q/gain_k: fp32 device arrays, [128]
  * shared by all heads when gain_head_stride == 0, else [H, gain_head_stride].
- * Errors: EINVAL for null/misaligned pointers, strides < H*128 or not
- * multiples of 8, eps < 0 or not finite, partial overlap. */
+ * q_in and q_out may both be NULL: then only k is processed (gain_q is
+ * ignored), for use with h3attn_forward_fused_q, which applies the same
+ * arithmetic to q itself.
+ * Errors: EINVAL for null/misaligned pointers (or only one of q_in/q_out
+ * NULL), strides < H*128 or not multiples of 8, eps < 0 or not finite,
+ * partial overlap. */
 h3attn_status h3attn_qk_prologue(h3attn_plan_t plan, const void* q_in, const void* k_in,
                                  int64_t in_row_stride, void* q_out, void* k_out,
                                  int64_t out_row_stride, const float* gain_q,
@@ -154,6 +158,22 @@ h3attn_status h3attn_qk_prologue(h3attn_plan_t plan, const void* q_in, const voi
 h3attn_status h3attn_forward(h3attn_plan_t plan, const void* q, const void* k, const void* v,
                              int64_t qkv_row_stride, void* o, int64_t o_row_stride,
                              float softmax_scale, float* lse_out, void* cuda_stream);
+
+/* The same attention with the Q half of the prologue fused in ([SPARK] "What
+ * this config does": Q RMSNorm + rot96 RoPE fused into one kernel).  q_raw
+ * holds the raw queries (bf16 [S,H,128], qkv_row_stride); each query tile is
+ * normalised with gain_q (layout as in h3attn_qk_prologue) and eps and
+ * rotated with the plan's table in shared memory, with arithmetic identical
+ * to h3attn_qk_prologue's (the q̂ values, and so o and lse, are bit-identical
+ * to h3attn_qk_prologue followed by h3attn_forward).  q_raw is only read (it
+ * may be the q part of a fused qkv buffer); k must already be k̂ (e.g.
+ * h3attn_qk_prologue with q_in = q_out = NULL).  Other arguments and errors as
+ * h3attn_forward, plus EINVAL for a NULL or misaligned gain_q, a bad
+ * gain_head_stride, or eps < 0 or not finite. */
+h3attn_status h3attn_forward_fused_q(h3attn_plan_t plan, const void* q_raw, const void* k, const void* v,
+                                     int64_t qkv_row_stride, void* o, int64_t o_row_stride,
+                                     const float* gain_q, int64_t gain_head_stride, float eps,
+                                     float softmax_scale, float* lse_out, void* cuda_stream);
 
 /* Allocation-free forward.  The pages have no counterpart: this entry point
  * exists for callers that may not allocate device memory -- code whose device

@@ -15,14 +15,18 @@
 // CTA holds only half of every B operand -- keys [64 rank, 64 rank + 64) of a
 // K tile and dims [64 rank, 64 rank + 64) of a V tile -- so a CTA reads
 // (and loads from L2) half the key/value bytes a single-CTA kernel would.
-// Per CTA, 10 warps:
-//   warp 9       TMA producer: its own Q tiles, then its halves of the
-//                document's K and V tiles through an 8-slot ring; V(j) and the
-//                next K tile form one group behind one barrier.
+// Per CTA, 11 warps:
+//   warp 9       TMA producer: its own Q tiles (double buffered: the next
+//                unit's behind the current unit's first K/V group), and its
+//                halves of the document's K and V tiles through a 6-slot ring;
+//                V(j) and the next K tile form one group behind one barrier.
+//   warp 10      Q warp: as each Q tile lands, applies the fused Q prologue
+//                in place when asked (RMSNorm with gain, rot96 rotation) and
+//                reports the tile ready to the even CTA.  Q tiles are double
+//                buffered, so the next unit's tiles are ready before it starts.
 //   warp 8       even CTA: MMA issuer for the pair, S_s = Q_s K_j^T and
-//                O_s += P_s V_j, fp32 accumulators in TMEM; odd CTA: relays
-//                the arrival of its Q tiles to the even CTA's barriers.  Both
-//                allocate the pair's TMEM together.
+//                O_s += P_s V_j, fp32 accumulators in TMEM.  Both CTAs'
+//                warp 8 allocate the pair's TMEM together.
 //   warps 0..3   softmax for query tile 0 of this CTA,
 //   warps 4..7   softmax for query tile 1: one thread per query row reads its
 //                S row from TMEM, keeps the running max and sum in registers,
@@ -49,8 +53,7 @@
 // each CTA arrives only once its CTA's next K/V group has landed; a softmax
 // thread that sees S of key tile t ready frees the ring slots of the group
 // holding K(t) (everything before that QK has completed).  Q tiles: the even
-// CTA's "full" barrier expects one more arrival, made by the odd CTA's relay
-// once the odd CTA's tile has landed.
+// CTA's "Q ready" barrier counts one arrival from the Q warp of each CTA.
 //
 // Every mbarrier wait is bounded: on expiry the CTA raises an abort flag,
 // records a timeout in the device error word, drains its own copies and MMAs
@@ -61,32 +64,34 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
-#include <cstdio>
 
 #include "device_common.cuh"
+#include "qk_norm.cuh"
 
 namespace h3 {
 
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kMmaWarp = 8;
 constexpr int kTmaWarp = 9;
+constexpr int kQWarp = 10;
 constexpr int kTileRows = 128;
-constexpr int kSlots = 8;                              // ring slots (16 KB each)
+constexpr int kSlots = 6;                              // ring slots (16 KB each)
 constexpr int kGroups = kSlots / 2;                    // key/value groups in flight
 constexpr uint32_t kQTileBytes = 128 * 128 * 2;        // 32 KB, two 16 KB halves
 constexpr uint32_t kQHalfBytes = kQTileBytes / 2;
 constexpr uint32_t kSlotBytes = 64 * 128 * 2;          // 16 KB
 constexpr uint32_t kKHalfBytes = kSlotBytes / 2;       // 64 keys x 64 dims
-constexpr uint32_t kSmemQ = 0;                         // 2 tiles
-constexpr uint32_t kSmemKV = 2 * kQTileBytes;          // kSlots slots
+constexpr uint32_t kSmemQ = 0;                         // 2 buffers x 2 query tiles
+constexpr uint32_t kSmemKV = 4 * kQTileBytes;          // kSlots slots
 constexpr uint32_t kSmemBar = kSmemKV + kSlots * kSlotBytes;
-// barriers: q_full[2] q_empty[2] kv_full[G] kv_empty[G] s_ready[2] p_ready[2] o_ready[2] drain
-constexpr int kNumBars = 2 + 2 + kGroups + kGroups + 2 + 2 + 2 + 1;
+// barriers: q_full[4] q_empty[4] q_ready[4] kv_full[G] kv_empty[G] s_ready[2] p_ready[2] o_ready[2] drain
+constexpr int kNumBars = 12 + 2 * kGroups + 2 + 2 + 2 + 1;
 constexpr uint32_t kSmemMisc = kSmemBar + kNumBars * 8;
 constexpr uint32_t kSmemBytes = kSmemMisc + 16;
 constexpr size_t kSmemAlloc = kSmemBytes + 1024;       // slack to align the base to 1 KB
+static_assert(kSmemAlloc <= 227 * 1024, "shared memory per CTA");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 2000000000ull;         // 2 s
 constexpr float kRescaleThreshold = 8.0f;              // log2 units: rescale when max grows by > 2^8
@@ -98,16 +103,18 @@ constexpr uint32_t kIdescBase = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3
 constexpr uint32_t kIdescQK = kIdescBase;              // A, B K-major
 constexpr uint32_t kIdescPV = kIdescBase | (1u << 16);  // B (V) MN-major
 
+// Q slot i = 2 * buffer + query tile; the unit with ordinal k (per pair) uses buffer k & 1.
 struct Bars {
   uint32_t base;
-  __device__ uint32_t q_full(int s) const { return base + 8 * s; }
-  __device__ uint32_t q_empty(int s) const { return base + 8 * (2 + s); }
-  __device__ uint32_t kv_full(int i) const { return base + 8 * (4 + i); }
-  __device__ uint32_t kv_empty(int i) const { return base + 8 * (4 + kGroups + i); }
-  __device__ uint32_t s_ready(int s) const { return base + 8 * (4 + 2 * kGroups + s); }
-  __device__ uint32_t p_ready(int s) const { return base + 8 * (6 + 2 * kGroups + s); }
-  __device__ uint32_t o_ready(int s) const { return base + 8 * (8 + 2 * kGroups + s); }
-  __device__ uint32_t drain() const { return base + 8 * (10 + 2 * kGroups); }
+  __device__ uint32_t q_full(int i) const { return base + 8 * i; }
+  __device__ uint32_t q_empty(int i) const { return base + 8 * (4 + i); }
+  __device__ uint32_t q_ready(int i) const { return base + 8 * (8 + i); }
+  __device__ uint32_t kv_full(int i) const { return base + 8 * (12 + i); }
+  __device__ uint32_t kv_empty(int i) const { return base + 8 * (12 + kGroups + i); }
+  __device__ uint32_t s_ready(int s) const { return base + 8 * (12 + 2 * kGroups + s); }
+  __device__ uint32_t p_ready(int s) const { return base + 8 * (14 + 2 * kGroups + s); }
+  __device__ uint32_t o_ready(int s) const { return base + 8 * (16 + 2 * kGroups + s); }
+  __device__ uint32_t drain() const { return base + 8 * (18 + 2 * kGroups); }
 };
 
 struct UnitGeom {
@@ -224,6 +231,81 @@ __device__ __forceinline__ void load_scores(uint32_t t_s, uint32_t (&r)[4][32], 
   }
 }
 
+// Fused Q prologue for one query row held in shared memory (128-byte swizzled
+// K-major tile, two 16 KB halves): RMSNorm with gain and the rot96 rotation,
+// in place, with the arithmetic of qk_norm.cuh (the same bits as the
+// separate prologue kernel).  Rare (once per row per unit), so kept out of line.
+static __device__ __noinline__ void norm_rope_q_row(uint32_t tile, uint32_t r, const float* gain,
+                                                    const float2* rope_row, float eps) {
+  auto chunk = [&](int c) {  // shared address of dims [8c, 8c + 8) of row r
+    return tile + (uint32_t)(c >> 3) * kQHalfBytes + r * 128u + ((((uint32_t)c & 7u) ^ (r & 7u)) << 4);
+  };
+  auto ld = [&](int c) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(chunk(c)));
+    return v;
+  };
+  auto st = [&](int c, const uint4& v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(chunk(c)), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+  };
+  float p[16];
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    float x[8];
+    qkn::unpack8(ld(c), x);
+    p[c] = qkn::chunk_ss(x);
+  }
+  const float rr = qkn::inv_rms(qkn::tree16(p), eps);
+#pragma unroll 1
+  for (int c = 0; c < 6; ++c) {
+    float xa[8], xb[8], ya[8], yb[8], cs[8], sn[8];
+    qkn::unpack8(ld(c), xa);
+    qkn::unpack8(ld(c + 6), xb);
+    const float4* ga = reinterpret_cast<const float4*>(gain + 8 * c);
+    const float4* gb = reinterpret_cast<const float4*>(gain + 48 + 8 * c);
+    const float4 a0 = __ldg(ga), a1 = __ldg(ga + 1), b0 = __ldg(gb), b1 = __ldg(gb + 1);
+    const float gav[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const float gbv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+    const float4* t = reinterpret_cast<const float4*>(rope_row + 8 * c);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 v = __ldg(t + i);  // (cos, sin) of two consecutive angles
+      cs[2 * i] = v.x;
+      sn[2 * i] = v.y;
+      cs[2 * i + 1] = v.z;
+      sn[2 * i + 1] = v.w;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      ya[e] = qkn::scale_gain(xa[e], rr, gav[e]);
+      yb[e] = qkn::scale_gain(xb[e], rr, gbv[e]);
+    }
+    float oa[8], ob[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      oa[e] = qkn::rot_lo(ya[e], yb[e], cs[e], sn[e]);
+      ob[e] = qkn::rot_hi(yb[e], ya[e], cs[e], sn[e]);
+    }
+    st(c, qkn::pack8(oa));
+    st(c + 6, qkn::pack8(ob));
+  }
+#pragma unroll 1
+  for (int c = 12; c < 16; ++c) {
+    float x[8];
+    qkn::unpack8(ld(c), x);
+    const float4* g = reinterpret_cast<const float4*>(gain + 8 * c);
+    const float4 g0 = __ldg(g), g1 = __ldg(g + 1);
+    const float gv[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = qkn::scale_gain(x[e], rr, gv[e]);
+    st(c, qkn::pack8(x));
+  }
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, ForwardArgs a) {
@@ -242,9 +324,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
+    for (int i = 0; i < 4; ++i) {
+      dev::mbar_init(bars.q_full(i), 1);
+      dev::mbar_init(bars.q_empty(i), 1);
+      dev::mbar_init(bars.q_ready(i), 2);           // the Q warp of each CTA of the pair
+    }
     for (int s = 0; s < 2; ++s) {
-      dev::mbar_init(bars.q_full(s), rank == 0 ? 2 : 1);  // even CTA: own copies + the odd CTA's relay
-      dev::mbar_init(bars.q_empty(s), 1);
       dev::mbar_init(bars.s_ready(s), 1);
       dev::mbar_init(bars.p_ready(s), 8);           // one arrival per softmax warp of the pair
       dev::mbar_init(bars.o_ready(s), 1);
@@ -277,27 +362,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint64_t pol_q = dev::policy_evict_first();
       const uint64_t pol_kv = dev::policy_evict_last();
-      uint32_t grp = 0, q_it[2] = {0, 0};
+      uint32_t grp = 0, q_use[4] = {0, 0, 0, 0};
       bool ok = true;
-      for (int u = pair; ok && u < a.n_units; u += n_pairs) {
-        const UnitGeom g = unit_geom(a.units, u);
+      // Q tiles of the unit with ordinal k, into buffer k & 1 (the slot is
+      // freed by the MMA after the last QK of the unit two before).
+      auto load_q = [&](const UnitGeom& g, int k) {
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
           if (!ok || s >= g.n_st) break;
-          ok = dev::mbar_wait(bars.q_empty(s), (q_it[s] & 1) ^ 1, abort_flag, a.err, kTimeoutNs);
+          const int i = 2 * (k & 1) + s;
+          ok = dev::mbar_wait(bars.q_empty(i), (q_use[i] & 1) ^ 1, abort_flag, a.err, kTimeoutNs);
           if (!ok) break;
-          const uint32_t dst = sbase + kSmemQ + s * kQTileBytes;
-          dev::mbar_arrive_expect_tx(bars.q_full(s), kQTileBytes);
+          const uint32_t dst = sbase + kSmemQ + i * kQTileBytes;
+          dev::mbar_arrive_expect_tx(bars.q_full(i), kQTileBytes);
           const int32_t row = g.q0 + s * 2 * kTileRows + (int32_t)rank * kTileRows;
-          dev::tma_load_2d(dst, &tm_q, bars.q_full(s), g.head * 128, row, pol_q);
-          dev::tma_load_2d(dst + kQHalfBytes, &tm_q, bars.q_full(s), g.head * 128 + 64, row, pol_q);
-          ++q_it[s];
+          dev::tma_load_2d(dst, &tm_q, bars.q_full(i), g.head * 128, row, pol_q);
+          dev::tma_load_2d(dst + kQHalfBytes, &tm_q, bars.q_full(i), g.head * 128 + 64, row, pol_q);
+          ++q_use[i];
         }
+      };
+      int k = 0;
+      for (int u = pair; ok && u < a.n_units; u += n_pairs, ++k) {
+        const UnitGeom g = unit_geom(a.units, u);
+        const bool has_next = u + n_pairs < a.n_units;
         // Key/value groups: group 0 is the first unit's first K tile (ring slot
         // 0); group n >= 1 is V(j) with the next K tile -- K(j+1), or the next
         // unit's first K tile -- in slots (2n-1) % kSlots and 2n % kSlots, one
         // full and one empty barrier (index n % kGroups) for both.
-        if (u == pair) {
+        if (k == 0) {
+          load_q(g, 0);
+          if (!ok) break;
           ok = dev::mbar_wait(bars.kv_empty(0), 1, abort_flag, a.err, kTimeoutNs);
           if (!ok) break;
           dev::mbar_arrive_expect_tx(bars.kv_full(0), kSlotBytes);
@@ -308,7 +402,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           bool has_k = j + 1 < g.hi;
           int k_head = g.head;
           int32_t k_row = g.kv0 + (j + 1) * kTileRows;
-          if (!has_k && u + n_pairs < a.n_units) {
+          if (!has_k && has_next) {
             const UnitGeom n = unit_geom(a.units, u + n_pairs);
             has_k = true;
             k_head = n.head;
@@ -324,61 +418,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             load_k_half(sbase + kSmemKV + ((2 * grp) % kSlots) * kSlotBytes, &tm_k, bars.kv_full(b), k_head,
                         k_row, rank, pol_kv);
           ++grp;
+          // the next unit's Q tiles, behind this unit's first group
+          if (j == g.lo && has_next) load_q(unit_geom(a.units, u + n_pairs), k + 1);
         }
       }
       if (!ok) {
         // drain: wait (bounded) for every copy this thread issued into the ring and Q
-        // (the even CTA's Q barriers also need the relay's arrival: a wait
-        // that times out here only delays the exit)
         for (uint32_t r = 1; r <= (uint32_t)kGroups && r <= grp; ++r) {
           const uint32_t n = grp - r;
           dev::mbar_wait_bounded(bars.kv_full(n % kGroups), (n / kGroups) & 1, nullptr, nullptr, kTimeoutNs);
         }
 #pragma unroll
-        for (int s = 0; s < 2; ++s)
-          if (q_it[s])
-            dev::mbar_wait_bounded(bars.q_full(s), (q_it[s] - 1) & 1, nullptr, nullptr, kTimeoutNs);
-      }
-    }
-  } else if (warp == kMmaWarp && rank != 0) {
-    // ------------------------------------------- relay (odd CTA of the pair) ----
-    // As each of this CTA's Q tiles lands (and, before the first, the first K
-    // group), arrives on the even CTA's matching barrier.
-    if (lane == 0) {
-      uint32_t q_it[2] = {0, 0};
-      bool ok = dev::mbar_wait(bars.kv_full(0), 0, abort_flag, a.err, kTimeoutNs);
-      for (int u = pair; ok && u < a.n_units; u += n_pairs) {
-        const UnitGeom g = unit_geom(a.units, u);
-#pragma unroll
-        for (int s = 0; s < 2; ++s) {
-          if (!ok || s >= g.n_st) break;
-          ok = dev::mbar_wait(bars.q_full(s), q_it[s] & 1, abort_flag, a.err, kTimeoutNs);
-          if (!ok) break;
-          ++q_it[s];
-          dev::mbar_arrive_cluster(dev::mapa_shared(bars.q_full(s), 0));
-        }
+        for (int i = 0; i < 4; ++i)
+          if (q_use[i]) dev::mbar_wait_bounded(bars.q_full(i), (q_use[i] - 1) & 1, nullptr, nullptr, kTimeoutNs);
       }
     }
   } else if (warp == kMmaWarp) {
     // ----------------------------------------- MMA issuer (even CTA, pair) ----
-    if (lane == 0) {
-      uint32_t grp = 0, q_it0 = 0, q_it1 = 0, p_it0 = 0, p_it1 = 0;
+    if (lane == 0 && rank == 0) {
+      uint32_t grp = 0, q_use[4] = {0, 0, 0, 0}, p_it0 = 0, p_it1 = 0;
       bool ok = true;
       bool issued = false;
-      for (int u = pair; ok && u < a.n_units; u += n_pairs) {
+      int k = 0;
+      for (int u = pair; ok && u < a.n_units; u += n_pairs, ++k) {
         const UnitGeom g = unit_geom(a.units, u);
-        ok = dev::mbar_wait(bars.q_full(0), q_it0 & 1, abort_flag, a.err, kTimeoutNs);
-        ++q_it0;
-        if (ok && g.n_st > 1) {
-          ok = dev::mbar_wait(bars.q_full(1), q_it1 & 1, abort_flag, a.err, kTimeoutNs);
-          ++q_it1;
+        const uint32_t qb = 2 * (k & 1);
+        // Q tiles of this unit, prepared in both CTAs (and, for the first
+        // unit, the first K group landed in both)
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          if (!ok || s >= g.n_st) break;
+          ok = dev::mbar_wait(bars.q_ready(qb + s), q_use[qb + s] & 1, abort_flag, a.err, kTimeoutNs);
+          ++q_use[qb + s];
         }
-        // this unit's first K tile: group 0 (first unit; the odd CTA's half is
-        // covered by its relay's Q arrival) or the K half of the previous
+        // this unit's first K tile: group 0, or the K half of the previous
         // unit's last group (covered by that unit's last P-ready barrier)
         uint32_t k0;
-        if (u == pair) {
-          if (ok) ok = dev::mbar_wait(bars.kv_full(0), 0, abort_flag, a.err, kTimeoutNs);
+        if (k == 0) {
           k0 = 0;
           grp = 1;
         } else {
@@ -389,9 +465,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
           if (s >= g.n_st) break;
-          issue_qk(tmem + s * 128, sbase + kSmemQ + s * kQTileBytes, sbase + kSmemKV + k0 * kSlotBytes);
+          issue_qk(tmem + s * 128, sbase + kSmemQ + (qb + s) * kQTileBytes, sbase + kSmemKV + k0 * kSlotBytes);
           dev::mma_commit_pair_mc(bars.s_ready(s), kPairMask);
-          if (g.hi - g.lo == 1) dev::mma_commit_pair_mc(bars.q_empty(s), kPairMask);
+          if (g.hi - g.lo == 1) dev::mma_commit_pair_mc(bars.q_empty(qb + s), kPairMask);
         }
         issued = true;
         for (int j = g.lo; j < g.hi; ++j) {
@@ -409,9 +485,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             dev::tc_fence_after();
             issue_pv(tmem + 256 + s * 128, tmem + s * 128, sbase + kSmemKV + vslot * kSlotBytes, j > g.lo);
             if (more) {
-              issue_qk(tmem + s * 128, sbase + kSmemQ + s * kQTileBytes, sbase + kSmemKV + kslot * kSlotBytes);
+              issue_qk(tmem + s * 128, sbase + kSmemQ + (qb + s) * kQTileBytes,
+                       sbase + kSmemKV + kslot * kSlotBytes);
               dev::mma_commit_pair_mc(bars.s_ready(s), kPairMask);
-              if (j + 2 == g.hi) dev::mma_commit_pair_mc(bars.q_empty(s), kPairMask);
+              if (j + 2 == g.hi) dev::mma_commit_pair_mc(bars.q_empty(qb + s), kPairMask);
             } else {
               dev::mma_commit_pair_mc(bars.o_ready(s), kPairMask);
             }
@@ -426,6 +503,42 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         dev::mbar_wait_bounded(bars.drain(), 0, nullptr, nullptr, kTimeoutNs);
       }
     }
+  } else if (warp == kQWarp) {
+    // ----------------------------------------------------------- Q warp ----
+    // As each of this CTA's Q tiles lands: with the fused Q prologue,
+    // normalise and rotate its rows in place (lane l takes rows l, l+32, ...);
+    // then report the tile ready to the even CTA.  Before the first unit's
+    // first tile, the first K group must have landed too.
+    uint32_t q_use[4] = {0, 0, 0, 0};
+    bool ok = true;
+    const bool fuse_q = a.gain_q != nullptr;
+    int k = 0;
+    for (int u = pair; ok && u < a.n_units; u += n_pairs, ++k) {
+      const UnitGeom g = unit_geom(a.units, u);
+#pragma unroll 1
+      for (int s = 0; s < 2 && s < g.n_st; ++s) {
+        const int i = 2 * (k & 1) + s;
+        bool good = dev::mbar_wait(bars.q_full(i), q_use[i] & 1, abort_flag, a.err, kTimeoutNs);
+        ++q_use[i];
+        if (good && fuse_q) {
+          const int32_t row0 = g.q0 + s * 2 * kTileRows + (int32_t)rank * kTileRows;
+          const float* gain = a.gain_q + (int64_t)g.head * a.gain_head_stride;
+#pragma unroll 1
+          for (uint32_t r = lane; r < (uint32_t)kTileRows; r += 32) {
+            const int32_t row = row0 + (int32_t)r;
+            if (row < g.kv1)
+              norm_rope_q_row(sbase + kSmemQ + i * kQTileBytes, r, gain, a.rope + (int64_t)row * kRopeHalf, a.eps);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor cores
+        }
+        __syncwarp();
+        if (good && k == 0 && s == 0 && lane == 0)
+          good = dev::mbar_wait(bars.kv_full(0), 0, abort_flag, a.err, kTimeoutNs);
+        if (lane == 0) dev::mbar_arrive_cluster(dev::mapa_shared(bars.q_ready(i), 0));
+        ok = __all_sync(0xffffffffu, good);
+        if (!ok) break;
+      }
+    }
   } else {
     // ---------------------------------------------------------- softmax ----
     const int st = warp >> 2;            // query tile of this warpgroup
@@ -434,6 +547,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t t_s = tmem + (lane_base << 16) + st * 128;        // S_s / P_s
     const uint32_t t_o = tmem + (lane_base << 16) + 256 + st * 128;  // O_s
     const uint32_t p_ready_remote = dev::mapa_shared(bars.p_ready(st), 0);
+    const bool lead_lane = (warp & 3) == 0 && lane == 0;             // one lane per warpgroup
     uint32_t s_it = 0, o_it = 0;
     uint32_t t0 = 0;                     // key tiles the pair has started before this unit
     bool ok = true;
@@ -445,8 +559,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       t0 += g.hi - g.lo;
       if (st >= g.n_st) continue;
       // ring bookkeeping by one lane of one warp per CTA
-      const bool releases = (warp & 3) == 0 && lane == 0 && st == g.n_st - 1;
-      const bool checks_kv = (warp & 3) == 0 && lane == 0 && st == 0;
+      const bool releases = lead_lane && st == g.n_st - 1;
+      const bool checks_kv = lead_lane && st == 0;
       float m_used = -INFINITY, l = 0.f;
       for (int j = g.lo; j < g.hi; ++j) {
         const uint32_t t = t_unit + (j - g.lo);  // the pair's running key-tile count

@@ -256,10 +256,13 @@ h3attn_status h3attn_qk_prologue(h3attn_plan_t plan, const void* q_in, const voi
                                  void* cuda_stream) {
   clear_error();
   if (h3attn_status s = check_plan(plan)) return s;
-  if (!q_in || !k_in || !q_out || !k_out || !gain_q || !gain_k)
+  // q_in and q_out both NULL: k only (the queries go to h3attn_forward_fused_q)
+  const bool with_q = q_in != nullptr || q_out != nullptr;
+  if (with_q && (!q_in || !q_out)) return fail(H3ATTN_EINVAL, "q_in and q_out must both be set or both NULL");
+  if (!k_in || !k_out || !gain_k || (with_q && !gain_q))
     return fail(H3ATTN_EINVAL, "NULL tensor or gain pointer");
-  if (!aligned16(q_in) || !aligned16(k_in) || !aligned16(q_out) || !aligned16(k_out) ||
-      !aligned16(gain_q) || !aligned16(gain_k))
+  if (!aligned16(k_in) || !aligned16(k_out) || !aligned16(gain_k) ||
+      (with_q && (!aligned16(q_in) || !aligned16(q_out) || !aligned16(gain_q))))
     return fail(H3ATTN_EINVAL, "tensors and gains must be 16-byte aligned");
   const int64_t width = (int64_t)plan->num_heads * kHeadDim;
   if (in_row_stride < width || out_row_stride < width || (in_row_stride % 8) || (out_row_stride % 8))
@@ -274,10 +277,10 @@ h3attn_status h3attn_qk_prologue(h3attn_plan_t plan, const void* q_in, const voi
   struct T { const void* p; int64_t s; };
   const T ins[2] = {{q_in, in_row_stride}, {k_in, in_row_stride}};
   const T outs[2] = {{q_out, out_row_stride}, {k_out, out_row_stride}};
-  if (may_overlap(q_out, out_row_stride, k_out, out_row_stride, S, H))
+  if (with_q && may_overlap(q_out, out_row_stride, k_out, out_row_stride, S, H))
     return fail(H3ATTN_EINVAL, "q_out and k_out overlap");
-  for (int o = 0; o < 2; ++o)
-    for (int i = 0; i < 2; ++i) {
+  for (int o = with_q ? 0 : 1; o < 2; ++o)
+    for (int i = with_q ? 0 : 1; i < 2; ++i) {
       const bool same = (outs[o].p == ins[i].p && outs[o].s == ins[i].s && o == i);
       if (!same && may_overlap(outs[o].p, outs[o].s, ins[i].p, ins[i].s, S, H))
         return fail(H3ATTN_EINVAL, "%s_out overlaps %s_in other than exactly in place",
@@ -286,17 +289,16 @@ h3attn_status h3attn_qk_prologue(h3attn_plan_t plan, const void* q_in, const voi
   DeviceGuard g;
   cudaError_t e = g.enter(plan->device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
-  PrologueArgs a{q_in, k_in, q_out, k_out, in_row_stride, out_row_stride, gain_q, gain_k,
-                 gain_head_stride, plan->d_rope, S, H, eps};
+  PrologueArgs a{with_q ? q_in : nullptr, k_in, with_q ? q_out : nullptr, k_out, in_row_stride, out_row_stride,
+                 gain_q, gain_k, gain_head_stride, plan->d_rope, S, H, eps};
   e = launch_qk_prologue(a, plan->num_sms, static_cast<cudaStream_t>(cuda_stream));
   return e == cudaSuccess ? H3ATTN_OK : cuda_fail(e, "qk_prologue launch");
 }
 
-h3attn_status h3attn_forward(h3attn_plan_t plan, const void* q, const void* k, const void* v,
-                             int64_t qkv_row_stride, void* o, int64_t o_row_stride,
-                             float softmax_scale, float* lse_out, void* cuda_stream) {
-  clear_error();
-  if (h3attn_status s = check_plan(plan)) return s;
+static h3attn_status forward_impl(h3attn_plan_t plan, const void* q, const void* k, const void* v,
+                                  int64_t qkv_row_stride, void* o, int64_t o_row_stride, float softmax_scale,
+                                  float* lse_out, const float* gain_q, int64_t gain_head_stride, float eps,
+                                  void* cuda_stream) {
   if (!q || !k || !v || !o) return fail(H3ATTN_EINVAL, "NULL q/k/v/o pointer");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o))
     return fail(H3ATTN_EINVAL, "q/k/v/o must be 16-byte aligned");
@@ -324,7 +326,8 @@ h3attn_status h3attn_forward(h3attn_plan_t plan, const void* q, const void* k, c
   if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
   ForwardArgs a{q, k, v, o, lse_out, qkv_row_stride, o_row_stride, S, H,
                 softmax_scale * 1.4426950408889634f, plan->d_units, plan->n_units, plan->d_err,
-                plan->d_merges, (int32_t)plan->merges_host.size(), plan->d_part_o, plan->d_part_ml};
+                plan->d_merges, (int32_t)plan->merges_host.size(), plan->d_part_o, plan->d_part_ml,
+                gain_q, gain_head_stride, eps, plan->d_rope};
   std::string why;
   e = launch_forward(a, plan->device, plan->num_sms, static_cast<cudaStream_t>(cuda_stream), &why);
   if (e != cudaSuccess) {
@@ -332,6 +335,30 @@ h3attn_status h3attn_forward(h3attn_plan_t plan, const void* q, const void* k, c
     return cuda_fail(e, "forward launch");
   }
   return H3ATTN_OK;
+}
+
+h3attn_status h3attn_forward(h3attn_plan_t plan, const void* q, const void* k, const void* v,
+                             int64_t qkv_row_stride, void* o, int64_t o_row_stride,
+                             float softmax_scale, float* lse_out, void* cuda_stream) {
+  clear_error();
+  if (h3attn_status s = check_plan(plan)) return s;
+  return forward_impl(plan, q, k, v, qkv_row_stride, o, o_row_stride, softmax_scale, lse_out, nullptr, 0, 0.f,
+                      cuda_stream);
+}
+
+h3attn_status h3attn_forward_fused_q(h3attn_plan_t plan, const void* q_raw, const void* k, const void* v,
+                                     int64_t qkv_row_stride, void* o, int64_t o_row_stride,
+                                     const float* gain_q, int64_t gain_head_stride, float eps,
+                                     float softmax_scale, float* lse_out, void* cuda_stream) {
+  clear_error();
+  if (h3attn_status s = check_plan(plan)) return s;
+  if (!gain_q) return fail(H3ATTN_EINVAL, "NULL gain_q");
+  if (!aligned16(gain_q)) return fail(H3ATTN_EINVAL, "gain_q must be 16-byte aligned");
+  if (gain_head_stride != 0 && (gain_head_stride < kHeadDim || (gain_head_stride % 4)))
+    return fail(H3ATTN_EINVAL, "gain_head_stride must be 0 or >= 128 and a multiple of 4");
+  if (!std::isfinite(eps) || eps < 0.f) return fail(H3ATTN_EINVAL, "eps must be finite and >= 0");
+  return forward_impl(plan, q_raw, k, v, qkv_row_stride, o, o_row_stride, softmax_scale, lse_out, gain_q,
+                      gain_head_stride, eps, cuda_stream);
 }
 
 h3attn_status h3attn_get_device_error(h3attn_plan_t plan, void* cuda_stream) {

@@ -130,6 +130,13 @@ struct ForwardArgs {
   int32_t n_merges;
   float* part_o;
   float2* part_ml;
+  // Fused Q prologue (gain_q non-null): q holds the raw queries; the forward
+  // applies RMSNorm with gain and the rot96 rotation to each Q tile in shared
+  // memory, with the separate prologue's arithmetic.
+  const float* gain_q;
+  int64_t gain_head_stride;
+  float eps;
+  const float2* rope;          // [S, 48] (cos, sin)
 };
 // Work slots of the forward: CTA pairs that run at the same time on `device`
 // (the plan's segment list is balanced for this many).

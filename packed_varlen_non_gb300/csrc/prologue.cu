@@ -18,6 +18,7 @@
 #include <cuda_bf16.h>
 
 #include "device_common.cuh"
+#include "qk_norm.cuh"
 
 namespace h3 {
 
@@ -26,46 +27,31 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kRowsPerBlock = kThreads / 16;
 
-__device__ __forceinline__ void unpack8(const uint4& raw, float (&x)[8]) {
-  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    x[2 * i] = __uint_as_float(w[i] << 16);
-    x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-  }
-}
-
-__device__ __forceinline__ uint4 pack8(const float (&y)[8]) {
-  return make_uint4(dev::pack_bf16x2(y[0], y[1]), dev::pack_bf16x2(y[2], y[3]),
-                    dev::pack_bf16x2(y[4], y[5]), dev::pack_bf16x2(y[6], y[7]));
-}
-
-// Normalise x (this lane's 8 dims of one row), apply gain and the rotation.
+// Normalise x (this lane's 8 dims of one row), apply gain and the rotation
+// (the arithmetic of qk_norm.cuh, spread over 16 lanes).
 __device__ __forceinline__ void norm_rope(float (&x)[8], const float* gain, const float (&c)[8],
                                           const float (&s)[8], int lane16, unsigned mask,
                                           float eps) {
-  float ss = 0.f;
+  float ss = qkn::chunk_ss(x);
 #pragma unroll
-  for (int e = 0; e < 8; ++e) ss = fmaf(x[e], x[e], ss);
-#pragma unroll
-  for (int off = 8; off > 0; off >>= 1) ss += __shfl_xor_sync(mask, ss, off, 16);
-  const float r = rsqrtf(ss * (1.0f / kHeadDim) + eps);
+  for (int off = 8; off > 0; off >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(mask, ss, off, 16));
+  const float r = qkn::inv_rms(ss, eps);
   const float4 g0 = __ldg(reinterpret_cast<const float4*>(gain + lane16 * 8));
   const float4 g1 = __ldg(reinterpret_cast<const float4*>(gain + lane16 * 8 + 4));
   const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
   float y[8];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) y[e] = x[e] * r * g[e];
+  for (int e = 0; e < 8; ++e) y[e] = qkn::scale_gain(x[e], r, g[e]);
   const int partner = lane16 < 6 ? lane16 + 6 : (lane16 < 12 ? lane16 - 6 : lane16);
   float p[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) p[e] = __shfl_sync(mask, y[e], partner, 16);
   if (lane16 < 6) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = y[e] * c[e] - p[e] * s[e];
+    for (int e = 0; e < 8; ++e) x[e] = qkn::rot_lo(y[e], p[e], c[e], s[e]);
   } else if (lane16 < 12) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = y[e] * c[e] + p[e] * s[e];
+    for (int e = 0; e < 8; ++e) x[e] = qkn::rot_hi(y[e], p[e], c[e], s[e]);
   } else {
 #pragma unroll
     for (int e = 0; e < 8; ++e) x[e] = y[e];
@@ -81,14 +67,15 @@ __global__ void __launch_bounds__(kThreads) qk_prologue_kernel(PrologueArgs a) {
   const __nv_bfloat16* ki = static_cast<const __nv_bfloat16*>(a.k_in);
   __nv_bfloat16* qo = static_cast<__nv_bfloat16*>(a.q_out);
   __nv_bfloat16* ko = static_cast<__nv_bfloat16*>(a.k_out);
+  const bool with_q = a.q_in != nullptr;  // k only when q is handled by the forward
 #pragma unroll 1
   for (int64_t row = (int64_t)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 4); row < n_rows;
        row += step) {
     const int64_t tok = row / a.H;
     const int head = (int)(row - tok * a.H);
     const int64_t in_off = tok * a.in_stride + head * kHeadDim + lane16 * 8;
-    const uint4 qraw = __ldcs(reinterpret_cast<const uint4*>(qi + in_off));
     const uint4 kraw = __ldcs(reinterpret_cast<const uint4*>(ki + in_off));
+    const uint4 qraw = with_q ? __ldcs(reinterpret_cast<const uint4*>(qi + in_off)) : make_uint4(0, 0, 0, 0);
     float c[8], s[8];
     if (lane16 < 12) {
       const float4* t =
@@ -108,14 +95,17 @@ __global__ void __launch_bounds__(kThreads) qk_prologue_kernel(PrologueArgs a) {
         s[e] = 0.f;
       }
     }
-    float xq[8], xk[8];
-    unpack8(qraw, xq);
-    unpack8(kraw, xk);
-    norm_rope(xq, a.gain_q + head * a.gain_head_stride, c, s, lane16, mask, a.eps);
+    float xk[8];
+    qkn::unpack8(kraw, xk);
     norm_rope(xk, a.gain_k + head * a.gain_head_stride, c, s, lane16, mask, a.eps);
     const int64_t out_off = tok * a.out_stride + head * kHeadDim + lane16 * 8;
-    __stcs(reinterpret_cast<uint4*>(qo + out_off), pack8(xq));
-    __stcs(reinterpret_cast<uint4*>(ko + out_off), pack8(xk));
+    __stcs(reinterpret_cast<uint4*>(ko + out_off), qkn::pack8(xk));
+    if (with_q) {
+      float xq[8];
+      qkn::unpack8(qraw, xq);
+      norm_rope(xq, a.gain_q + head * a.gain_head_stride, c, s, lane16, mask, a.eps);
+      __stcs(reinterpret_cast<uint4*>(qo + out_off), qkn::pack8(xq));
+    }
   }
 }
 

@@ -54,6 +54,8 @@ _SIGS = {
                            c_void_p, c_void_p, c_int64, c_float, c_void_p],
     "h3attn_forward": [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_int64,
                        c_float, c_void_p, c_void_p],
+    "h3attn_forward_fused_q": [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_int64,
+                               c_void_p, c_int64, c_float, c_float, c_void_p, c_void_p],
     "h3attn_forward_noalloc": [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_int64,
                                c_void_p, c_int64, c_float, c_void_p, c_void_p],
     "h3attn_get_device_error": [c_void_p, c_void_p],
@@ -183,12 +185,14 @@ def h3attn_qk_prologue(plan, q_in, k_in, q_out, k_out, gain_q, gain_k, eps: floa
                        in_row_stride=None, out_row_stride=None, gain_head_stride: int = 0,
                        stream=None):
     """Tensors: bf16 [S, H, 128]-shaped views (row stride taken from dim 0)
-    or raw device pointers with explicit strides; gains fp32 on the device."""
+    or raw device pointers with explicit strides; gains fp32 on the device.
+    q_in = q_out = None processes k only (for h3attn_forward_fused_q)."""
     for pair in ((q_in, k_in, in_row_stride), (q_out, k_out, out_row_stride)):
-        if pair[2] is None and not isinstance(pair[0], int) and pair[0].stride(0) != pair[1].stride(0):
+        if (pair[2] is None and pair[0] is not None and not isinstance(pair[0], int)
+                and pair[0].stride(0) != pair[1].stride(0)):
             raise ValueError("q and k must share one row stride on each side")
-    _check(load().h3attn_qk_prologue(plan, _ptr(q_in), _ptr(k_in), _row_stride(q_in, in_row_stride),
-                                     _ptr(q_out), _ptr(k_out), _row_stride(q_out, out_row_stride),
+    _check(load().h3attn_qk_prologue(plan, _ptr(q_in), _ptr(k_in), _row_stride(k_in, in_row_stride),
+                                     _ptr(q_out), _ptr(k_out), _row_stride(k_out, out_row_stride),
                                      _ptr(gain_q), _ptr(gain_k), int(gain_head_stride), float(eps),
                                      _stream(stream)), "h3attn_qk_prologue")
 
@@ -202,6 +206,21 @@ def h3attn_forward(plan, q, k, v, o, softmax_scale: float, lse=None, qkv_row_str
     _check(load().h3attn_forward(plan, _ptr(q), _ptr(k), _ptr(v), _row_stride(q, qkv_row_stride),
                                  _ptr(o), _row_stride(o, o_row_stride), float(softmax_scale),
                                  _ptr(lse), _stream(stream)), "h3attn_forward")
+
+
+def h3attn_forward_fused_q(plan, q_raw, k, v, o, gain_q, softmax_scale: float, eps: float = 1e-6,
+                           lse=None, qkv_row_stride=None, o_row_stride=None, gain_head_stride: int = 0,
+                           stream=None):
+    """Forward with the Q prologue fused in: q_raw holds raw queries, k is
+    already k-hat (see include/h3attn.h)."""
+    if qkv_row_stride is None and not isinstance(q_raw, int):
+        strides = {int(x.stride(0)) for x in (q_raw, k, v)}
+        if len(strides) != 1:
+            raise ValueError(f"q, k and v must share one row stride (got {sorted(strides)})")
+    _check(load().h3attn_forward_fused_q(plan, _ptr(q_raw), _ptr(k), _ptr(v), _row_stride(q_raw, qkv_row_stride),
+                                         _ptr(o), _row_stride(o, o_row_stride), _ptr(gain_q),
+                                         int(gain_head_stride), float(eps), float(softmax_scale), _ptr(lse),
+                                         _stream(stream)), "h3attn_forward_fused_q")
 
 
 def h3attn_forward_noalloc(cu_seqlens, num_heads: int, q, k, v, o, softmax_scale: float, lse=None,

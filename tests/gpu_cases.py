@@ -48,8 +48,11 @@ class ProductResult:
 
 
 def run_product(docs, num_heads, t: synth.Tensors, eps=1e-6, scale=None, stream=None,
-                fused=False, want_lse=True, keep_device=False):
-    """Plan + prologue + forward through the C ABI; returns host copies."""
+                fused=False, want_lse=True, keep_device=False, fused_q=False):
+    """Plan + prologue + forward through the C ABI; returns host copies.
+    fused=True reads q/k/v from one fused-qkv buffer (prologue in place);
+    fused_q=True runs the k-only prologue and the forward with the Q prologue
+    fused in (q_hat is then not materialised: r.q_hat is None)."""
     scale = (1.0 / np.sqrt(128.0)) if scale is None else scale
     dev = torch.device("cuda")
     with H.Plan(docs, num_heads, stream=stream) as plan:
@@ -75,15 +78,20 @@ def run_product(docs, num_heads, t: synth.Tensors, eps=1e-6, scale=None, stream=
             k_hat = torch.empty_like(q_hat)
         o = torch.full((S, W), float("nan"), dtype=torch.bfloat16, device=dev)
         lse = torch.full((num_heads, S), float("nan"), dtype=torch.float32, device=dev) if want_lse else None
-        H.h3attn_qk_prologue(plan.handle, q_in, k_in, q_hat, k_hat, gq, gk, eps, stream=stream)
-        H.h3attn_forward(plan.handle, q_hat, k_hat, v, o, scale, lse, stream=stream)
+        if fused_q:
+            H.h3attn_qk_prologue(plan.handle, None, k_in, None, k_hat, None, gk, eps, stream=stream)
+            H.h3attn_forward_fused_q(plan.handle, q_in, k_hat, v, o, gq, scale, eps, lse, stream=stream)
+        else:
+            H.h3attn_qk_prologue(plan.handle, q_in, k_in, q_hat, k_hat, gq, gk, eps, stream=stream)
+            H.h3attn_forward(plan.handle, q_hat, k_hat, v, o, scale, lse, stream=stream)
         H.h3attn_get_device_error(plan.handle, stream=stream)
         r = ProductResult()
         r.S = S
-        r.q_hat = torch_bf16_to_f64(q_hat).reshape(S, num_heads, 128)
+        r.q_hat = None if fused_q else torch_bf16_to_f64(q_hat).reshape(S, num_heads, 128)
         r.k_hat = torch_bf16_to_f64(k_hat).reshape(S, num_heads, 128)
         r.o = torch_bf16_to_f64(o).reshape(S, num_heads, 128)
         r.o_bits = o.view(torch.int16).cpu().numpy()
+        r.k_bits = k_hat.view(torch.int16).cpu().numpy()
         r.lse = lse.cpu().numpy() if want_lse else None
         if keep_device:
             r.dev = dict(q_hat=q_hat, k_hat=k_hat, v=v, o=o)
