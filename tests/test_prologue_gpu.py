@@ -134,3 +134,28 @@ def test_prologue_rejects_bad_arguments(lib):
             H.h3attn_qk_prologue(p.handle, q, k, o1, o2, g, g, -1.0)
         with pytest.raises(H.H3AttnError):
             H.h3attn_qk_prologue(p.handle, q, k, o1, o2, g, g, 1e-6, in_row_stride=200, out_row_stride=256)
+
+
+@pytest.mark.parametrize("Hh,k_only", [(200, False), (21, True), (3, True)])
+def test_prologue_kernel_paths(lib, Hh, k_only):
+    # 200 heads (a wide token row); k only: the mode used with the fused-Q
+    # forward.  Both against the oracle, and k only byte-identical to the q+k
+    # call's k.
+    lens = [37, 130] if Hh == 200 else [700, 93, 1]
+    docs = [[(L, 1, 1, (0.0, 0.0, 0.0), (1.0, 0.0, 0.0))] for L in lens]
+    S, W = sum(lens), Hh * 128
+    t = random_tensors(S, Hh, seed=Hh + (7 if k_only else 0))
+    gq, gk = torch.from_numpy(t.gain_q).cuda(), torch.from_numpy(t.gain_k).cuda()
+    with H.Plan(docs, Hh) as p:
+        q = bf16_to_torch(t.q).view(S, W)
+        k = bf16_to_torch(t.k).view(S, W)
+        qo, ko = torch.empty_like(q), torch.empty_like(k)
+        _run(p, q, k, qo, ko, gq, gk)
+        yk = torch_bf16_to_f64(ko).reshape(S, Hh, 128)
+        check_prologue(yk, _oracle(docs, t.k, t.gain_k), f"k, {Hh} heads")
+        yq = torch_bf16_to_f64(qo).reshape(S, Hh, 128)
+        check_prologue(yq, _oracle(docs, t.q, t.gain_q), f"q, {Hh} heads")
+        if k_only:
+            ko2 = torch.empty_like(k)
+            _run(p, None, k, None, ko2, None, gk)
+            assert torch.equal(ko2.view(torch.int16), ko.view(torch.int16))
