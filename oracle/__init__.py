@@ -11,7 +11,9 @@ definitions on the pages:
 * ``oracle.prologue``   -- RMSNorm with gain, then NeoX rotate-half rotary on
                            dims 0..95 with angles from the position grid;
 * ``oracle.attention``  -- per-document bidirectional softmax attention,
-                           evaluated with a two-pass (max, then sum) softmax.
+                           evaluated with a two-pass (max, then sum) softmax;
+* ``oracle.fp8``        -- the FP8 (e4m3) variant: quantisers, dequantisation
+                           and the error bound of the kernel's P rounding.
 
 Pages cited (page title, then section):
   [PR26]   vllm.cpp PR #26 "feat(minimax-h3): port the MiniMax-H3 omni-modal
