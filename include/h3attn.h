@@ -175,6 +175,25 @@ h3attn_status h3attn_forward_fused_q(h3attn_plan_t plan, const void* q_raw, cons
                                      const float* gain_q, int64_t gain_head_stride, float eps,
                                      float softmax_scale, float* lse_out, void* cuda_stream);
 
+/* FP8 (e4m3) quantisation for h3attn_forward_fp8 ([PR26], [SPARK] "What this
+ * config does": a SageAttention2++-style low-precision attention; the pages
+ * give no scheme, this one is the plainest that runs both products on FP8
+ * tensor cores).  From q-hat, k-hat, v (bf16 [S,H,128], qkv_row_stride):
+ *   q8  [S,H,128] e4m3, scale sq [H,S] per (token, head) row;
+ *   k8  [S,H,128] e4m3, scale sk [H,S] per (head, 128-key tile of a document,
+ *       i.e. tokens [a + 128j, min(a + 128j + 128, b)) of document [a, b)),
+ *       stored for every token of the tile;
+ *   v8t [H,128,S_pad] e4m3 (S_pad = S rounded up to 16; channel-major, keys
+ *       contiguous), scale sv [H,128] per (head, channel) over all tokens.
+ * scale = amax / 448 (1 for an all-zero row, tile or channel); code =
+ * e4m3(x / scale), both divisions correctly rounded fp32, round to nearest
+ * even with saturation to +-448.  All outputs are device buffers owned by the
+ * caller, 16-byte aligned, not overlapping the inputs or each other.
+ * Errors: EINVAL for null/misaligned pointers, a bad stride, overlaps. */
+h3attn_status h3attn_fp8_quantize(h3attn_plan_t plan, const void* q_hat, const void* k_hat, const void* v,
+                                  int64_t qkv_row_stride, void* q8, void* k8, void* v8t, float* sq, float* sk,
+                                  float* sv, void* cuda_stream);
+
 /* Allocation-free forward.  The pages have no counterpart: this entry point
  * exists for callers that may not allocate device memory -- code whose device
  * memory is owned by a host framework's pool or arena (an engine plugin, a

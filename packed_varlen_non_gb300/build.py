@@ -26,7 +26,7 @@ NVCC = os.path.join(CUDA_HOME, "bin", "nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 HOST_SOURCES = ["plan.cpp", "capi.cpp"]
-CUDA_SOURCES = ["prologue.cu", "attn_fwd_tc.cu", "forward_noalloc.cu", "selftest.cu"]
+CUDA_SOURCES = ["prologue.cu", "attn_fwd_tc.cu", "forward_noalloc.cu", "selftest.cu", "fp8_quant.cu"]
 HEADERS = ["h3attn_internal.h", "device_common.cuh", "qk_norm.cuh"]
 
 _ELF_MACHINE = {"x86_64": 62, "aarch64": 183, "arm64": 183}

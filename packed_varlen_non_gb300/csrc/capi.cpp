@@ -85,6 +85,8 @@ void free_plan_device(Plan* p) {
   if (p->d_merges) cudaFree(p->d_merges);
   if (p->d_part_o) cudaFree(p->d_part_o);
   if (p->d_part_ml) cudaFree(p->d_part_ml);
+  if (p->d_ktiles) cudaFree(p->d_ktiles);
+  p->d_ktiles = nullptr;
   p->d_merges = nullptr;
   p->d_part_o = nullptr;
   p->d_part_ml = nullptr;
@@ -167,6 +169,7 @@ h3attn_status h3attn_plan_create(const h3attn_doc* docs, int32_t n_docs,
       (e = cudaMalloc(&p->d_rope, n_rope * sizeof(float2))) != cudaSuccess ||
       (e = cudaMalloc(&p->d_units, p->units_host.size() * sizeof(WorkUnit))) != cudaSuccess ||
       (e = cudaMalloc(&p->d_err, 16)) != cudaSuccess ||
+      (e = cudaMalloc(&p->d_ktiles, p->ktiles_host.size() * sizeof(int2))) != cudaSuccess ||
       (p->n_parts > 0 &&
        ((e = cudaMalloc(&p->d_merges, p->merges_host.size() * sizeof(MergeUnit))) != cudaSuccess ||
         (e = cudaMalloc(&p->d_part_o, (size_t)p->n_parts * kUnitRows * kHeadDim * sizeof(float))) != cudaSuccess ||
@@ -186,6 +189,8 @@ h3attn_status h3attn_plan_create(const h3attn_doc* docs, int32_t n_docs,
        (e = cudaMemcpyAsync(p->d_merges, p->merges_host.data(), p->merges_host.size() * sizeof(MergeUnit),
                             cudaMemcpyHostToDevice, st)) != cudaSuccess) ||
       (e = cudaMemsetAsync(p->d_err, 0, 16, st)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(p->d_ktiles, p->ktiles_host.data(), p->ktiles_host.size() * sizeof(int2),
+                           cudaMemcpyHostToDevice, st)) != cudaSuccess ||
       (e = cudaStreamSynchronize(st)) != cudaSuccess) {
     free_plan_device(p);
     delete p;
@@ -359,6 +364,48 @@ h3attn_status h3attn_forward_fused_q(h3attn_plan_t plan, const void* q_raw, cons
   if (!std::isfinite(eps) || eps < 0.f) return fail(H3ATTN_EINVAL, "eps must be finite and >= 0");
   return forward_impl(plan, q_raw, k, v, qkv_row_stride, o, o_row_stride, softmax_scale, lse_out, gain_q,
                       gain_head_stride, eps, cuda_stream);
+}
+
+h3attn_status h3attn_fp8_quantize(h3attn_plan_t plan, const void* q_hat, const void* k_hat, const void* v,
+                                  int64_t qkv_row_stride, void* q8, void* k8, void* v8t, float* sq, float* sk,
+                                  float* sv, void* cuda_stream) {
+  clear_error();
+  if (h3attn_status s = check_plan(plan)) return s;
+  if (!q_hat || !k_hat || !v || !q8 || !k8 || !v8t || !sq || !sk || !sv)
+    return fail(H3ATTN_EINVAL, "NULL tensor or scale pointer");
+  if (!aligned16(q_hat) || !aligned16(k_hat) || !aligned16(v) || !aligned16(q8) || !aligned16(k8) ||
+      !aligned16(v8t) || !aligned16(sq) || !aligned16(sk) || !aligned16(sv))
+    return fail(H3ATTN_EINVAL, "tensors and scales must be 16-byte aligned");
+  const int64_t width = (int64_t)plan->num_heads * kHeadDim;
+  if (qkv_row_stride < width || (qkv_row_stride % 8))
+    return fail(H3ATTN_EINVAL, "row stride must be >= H*128 = %lld and a multiple of 8", (long long)width);
+  const int64_t S = plan->S;
+  const int32_t H = plan->num_heads;
+  const int64_t s_pad = (S + 15) / 16 * 16;
+  // outputs must not share bytes with the inputs or with each other
+  const uintptr_t in_lo[3] = {reinterpret_cast<uintptr_t>(q_hat), reinterpret_cast<uintptr_t>(k_hat),
+                              reinterpret_cast<uintptr_t>(v)};
+  const uintptr_t in_len = (uintptr_t)(((S - 1) * qkv_row_stride + width) * 2);
+  const uintptr_t out_lo[6] = {reinterpret_cast<uintptr_t>(q8), reinterpret_cast<uintptr_t>(k8),
+                               reinterpret_cast<uintptr_t>(v8t), reinterpret_cast<uintptr_t>(sq),
+                               reinterpret_cast<uintptr_t>(sk), reinterpret_cast<uintptr_t>(sv)};
+  const uintptr_t out_len[6] = {(uintptr_t)(S * width), (uintptr_t)(S * width), (uintptr_t)(H * kHeadDim * s_pad),
+                                (uintptr_t)(H * S * 4), (uintptr_t)(H * S * 4), (uintptr_t)(H * kHeadDim * 4)};
+  for (int o = 0; o < 6; ++o) {
+    for (int i = 0; i < 3; ++i)
+      if (out_lo[o] < in_lo[i] + in_len && in_lo[i] < out_lo[o] + out_len[o])
+        return fail(H3ATTN_EINVAL, "an output overlaps an input");
+    for (int o2 = o + 1; o2 < 6; ++o2)
+      if (out_lo[o] < out_lo[o2] + out_len[o2] && out_lo[o2] < out_lo[o] + out_len[o])
+        return fail(H3ATTN_EINVAL, "two outputs overlap");
+  }
+  DeviceGuard g;
+  cudaError_t e = g.enter(plan->device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+  Fp8QuantArgs a{q_hat, k_hat, v, qkv_row_stride, S, H, plan->d_ktiles, (int32_t)plan->ktiles_host.size(),
+                 q8, k8, v8t, s_pad, sq, sk, sv};
+  e = launch_fp8_quantize(a, plan->num_sms, static_cast<cudaStream_t>(cuda_stream));
+  return e == cudaSuccess ? H3ATTN_OK : cuda_fail(e, "fp8 quantise launch");
 }
 
 h3attn_status h3attn_get_device_error(h3attn_plan_t plan, void* cuda_stream) {

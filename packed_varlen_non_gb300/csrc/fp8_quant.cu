@@ -1,0 +1,193 @@
+// Quantisation of the attention inputs to FP8 (e4m3) for the FP8 variant of
+// the forward: q-hat per (token, head) row, k-hat per (head, 128-key tile of a
+// document), v per (head, channel) over all tokens and written transposed
+// (channel-major, keys contiguous) for the PV product's K-major B operand.
+//
+// Pages: vllm.cpp PR #26 "feat(minimax-h3)" and the "h3-spark" model card,
+// "What this config does" name a SageAttention2++-style INT8/FP8 attention
+// without its scheme; this is the plainest scheme that runs both products on
+// FP8 tensor cores.  Every decision is made in fp32 -- scale = amax / 448 by
+// one correctly rounded division (1 for an all-zero row, tile or channel),
+// code = e4m3(x / scale) by one correctly rounded division and the hardware
+// round-to-nearest-even conversion with saturation -- so the codes are the
+// ones an fp32 reference computes.
+#include <cuda_bf16.h>
+
+#include "device_common.cuh"
+
+namespace h3 {
+
+namespace {
+
+constexpr float kE4m3Max = 448.0f;
+
+__device__ __forceinline__ float fp8_scale(float amax) { return amax > 0.f ? __fdiv_rn(amax, kE4m3Max) : 1.f; }
+
+// two e4m3 codes, lo in the low byte
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ void unpack8(const uint4& raw, float (&x)[8]) {
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    x[2 * i] = __uint_as_float(w[i] << 16);
+    x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+// 8 codes (one lane's 8 dims) as 8 bytes
+__device__ __forceinline__ uint2 codes8(const float (&x)[8], float s) {
+  uint32_t c[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) c[i] = e4m3x2(__fdiv_rn(x[2 * i], s), __fdiv_rn(x[2 * i + 1], s));
+  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
+// q-hat: 16 lanes per (token, head) row, 8 dims each.
+__global__ void __launch_bounds__(256) quant_rows_kernel(Fp8QuantArgs a) {
+  const int lane16 = threadIdx.x & 15;
+  const unsigned mask = 0xffffu << (threadIdx.x & 16);
+  const int64_t n_rows = a.S * a.H;
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.q_hat);
+  uint8_t* out = static_cast<uint8_t*>(a.q8);
+  for (int64_t row = (int64_t)blockIdx.x * 16 + (threadIdx.x >> 4); row < n_rows; row += (int64_t)gridDim.x * 16) {
+    const int64_t t = row / a.H;
+    const int h = (int)(row - t * a.H);
+    float f[8];
+    unpack8(__ldg(reinterpret_cast<const uint4*>(x + t * a.stride + h * kHeadDim + lane16 * 8)), f);
+    float m = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(f[e]));
+#pragma unroll
+    for (int off = 8; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(mask, m, off, 16));
+    const float s = fp8_scale(m);
+    *reinterpret_cast<uint2*>(out + row * kHeadDim + lane16 * 8) = codes8(f, s);
+    if (lane16 == 0) a.sq[(int64_t)h * a.S + t] = s;
+  }
+}
+
+// k-hat: one block per (key tile, head); thread i takes token b + i/2, dims
+// [64 (i%2), +64).
+__global__ void __launch_bounds__(256) quant_ktiles_kernel(Fp8QuantArgs a) {
+  __shared__ float warp_max[8];
+  const int tile = blockIdx.x, h = blockIdx.y;
+  const int2 te = a.tiles[tile];
+  const int64_t t = te.x + (threadIdx.x >> 1);
+  const bool live = t < te.y;
+  const int d0 = (threadIdx.x & 1) * 64;
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.k_hat) + t * a.stride + h * kHeadDim + d0;
+  float f[8][8];
+  float m = 0.f;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    if (live) {
+      unpack8(__ldg(reinterpret_cast<const uint4*>(x + c * 8)), f[c]);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[c][e] = 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(f[c][e]));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if ((threadIdx.x & 31) == 0) warp_max[threadIdx.x >> 5] = m;
+  __syncthreads();
+  m = warp_max[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) m = fmaxf(m, warp_max[w]);
+  const float s = fp8_scale(m);
+  if (!live) return;
+  uint8_t* out = static_cast<uint8_t*>(a.k8) + (t * a.H + h) * kHeadDim + d0;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) *reinterpret_cast<uint2*>(out + c * 8) = codes8(f[c], s);
+  if (d0 == 0) a.sk[(int64_t)h * a.S + t] = s;
+}
+
+// v, pass 1: per-(head, channel) amax over all tokens into the scale buffer's
+// bits (non-negative floats order like their bit patterns).
+constexpr int kVmaxTokens = 256;
+__global__ void __launch_bounds__(256) vmax_kernel(Fp8QuantArgs a) {
+  const int64_t t0 = (int64_t)blockIdx.x * kVmaxTokens;
+  const int64_t t1 = t0 + kVmaxTokens < a.S ? t0 + kVmaxTokens : a.S;
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.v);
+  uint32_t* bits = reinterpret_cast<uint32_t*>(a.sv);
+  for (int g = threadIdx.x; g < a.H * 16; g += blockDim.x) {  // groups of 8 channels
+    const int h = g >> 4, c0 = (g & 15) * 8;
+    float m[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int64_t t = t0; t < t1; ++t) {
+      float f[8];
+      unpack8(__ldg(reinterpret_cast<const uint4*>(x + t * a.stride + h * kHeadDim + c0)), f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) m[e] = fmaxf(m[e], fabsf(f[e]));
+    }
+#pragma unroll
+    for (int e = 0; e < 8; ++e) atomicMax(bits + h * kHeadDim + c0 + e, __float_as_uint(m[e]));
+  }
+}
+
+// v, pass 2: codes, transposed through shared memory: one block per (head,
+// 128-token chunk) writes v8t[h][c][t0 .. t0 + 128) for all 128 channels.
+__global__ void __launch_bounds__(256) vquant_kernel(Fp8QuantArgs a) {
+  __shared__ __align__(16) uint8_t tile[128][128 + 16];
+  const int h = blockIdx.y;
+  const int64_t t0 = (int64_t)blockIdx.x * 128;
+  const int tl = threadIdx.x >> 1, c0 = (threadIdx.x & 1) * 64;
+  const int64_t t = t0 + tl;
+  const uint32_t* bits = reinterpret_cast<const uint32_t*>(a.sv);
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.v) + t * a.stride + h * kHeadDim + c0;
+#pragma unroll 1
+  for (int c = 0; c < 64; c += 8) {
+    float f[8];
+    if (t < a.S) {
+      unpack8(__ldg(reinterpret_cast<const uint4*>(x + c)), f);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) f[e] = 0.f;
+    }
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {
+      const float s0 = fp8_scale(__uint_as_float(bits[h * kHeadDim + c0 + c + e]));
+      const float s1 = fp8_scale(__uint_as_float(bits[h * kHeadDim + c0 + c + e + 1]));
+      const uint32_t two = e4m3x2(__fdiv_rn(f[e], s0), __fdiv_rn(f[e + 1], s1));
+      tile[c0 + c + e][tl] = (uint8_t)(two & 0xff);
+      tile[c0 + c + e + 1][tl] = (uint8_t)(two >> 8);
+    }
+  }
+  __syncthreads();
+  // thread i writes channel i/2, tokens [64 (i%2), +64) as four 16-byte pieces
+  const int ch = threadIdx.x >> 1, k0 = (threadIdx.x & 1) * 64;
+  uint8_t* out = static_cast<uint8_t*>(a.v8t) + ((int64_t)h * kHeadDim + ch) * a.s_pad + t0 + k0;
+#pragma unroll
+  for (int p = 0; p < 4; ++p)
+    if (t0 + k0 + p * 16 < a.s_pad)
+      *reinterpret_cast<uint4*>(out + p * 16) = *reinterpret_cast<const uint4*>(&tile[ch][k0 + p * 16]);
+}
+
+__global__ void vscale_kernel(Fp8QuantArgs a) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < a.H * kHeadDim) a.sv[i] = fp8_scale(__uint_as_float(reinterpret_cast<const uint32_t*>(a.sv)[i]));
+}
+
+}  // namespace
+
+cudaError_t launch_fp8_quantize(const Fp8QuantArgs& a, int num_sms, cudaStream_t stream) {
+  if (a.S == 0) return cudaSuccess;
+  const int64_t n_rows = a.S * a.H;
+  const int64_t want = (n_rows + 15) / 16;
+  const int grid_rows = (int)(want < (int64_t)num_sms * 8 ? want : (int64_t)num_sms * 8);
+  quant_rows_kernel<<<grid_rows, 256, 0, stream>>>(a);
+  quant_ktiles_kernel<<<dim3(a.n_tiles, a.H), 256, 0, stream>>>(a);
+  cudaError_t e = cudaMemsetAsync(a.sv, 0, (size_t)a.H * kHeadDim * sizeof(float), stream);
+  if (e != cudaSuccess) return e;
+  vmax_kernel<<<(int)((a.S + kVmaxTokens - 1) / kVmaxTokens), 256, 0, stream>>>(a);
+  vquant_kernel<<<dim3((unsigned)((a.S + 127) / 128), a.H), 256, 0, stream>>>(a);
+  vscale_kernel<<<(a.H * kHeadDim + 255) / 256, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace h3

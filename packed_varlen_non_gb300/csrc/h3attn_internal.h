@@ -74,6 +74,7 @@ struct Plan {
   std::vector<WorkUnit> units_host;  // segment list (see build_segments)
   std::vector<MergeUnit> merges_host;
   int32_t n_parts = 0;
+  std::vector<int2> ktiles_host;     // (begin, end) of every document's 128-key tiles
 
   int32_t* d_cu = nullptr;
   float2* d_rope = nullptr;          // [S, 48] (cos, sin)
@@ -83,6 +84,7 @@ struct Plan {
   float* d_part_o = nullptr;         // [n_parts, kUnitRows, 128] unnormalised O
   float2* d_part_ml = nullptr;       // [n_parts, kUnitRows] (running max in log2 units, sum)
   uint32_t* d_err = nullptr;         // device error word
+  int2* d_ktiles = nullptr;
 };
 
 // Host-side plan construction (plan.cpp); returns an empty string or an error.
@@ -143,6 +145,26 @@ struct ForwardArgs {
 int forward_slots(int device, int num_sms);
 cudaError_t launch_forward(const ForwardArgs& a, int device, int num_sms, cudaStream_t stream,
                            std::string* why);
+
+// FP8 (e4m3) quantisation of q-hat, k-hat and v (fp8_quant.cu).
+struct Fp8QuantArgs {
+  const void* q_hat;
+  const void* k_hat;
+  const void* v;
+  int64_t stride;              // row stride of q-hat, k-hat, v (elements)
+  int64_t S;
+  int32_t H;
+  const int2* tiles;           // (begin, end) of every document's 128-key tiles
+  int32_t n_tiles;
+  void* q8;                    // [S, H, 128] codes
+  void* k8;                    // [S, H, 128] codes
+  void* v8t;                   // [H, 128, s_pad] codes, keys contiguous
+  int64_t s_pad;               // S rounded up to a multiple of 16
+  float* sq;                   // [H, S]
+  float* sk;                   // [H, S] (each token carries its tile's scale)
+  float* sv;                   // [H, 128]
+};
+cudaError_t launch_fp8_quantize(const Fp8QuantArgs& a, int num_sms, cudaStream_t stream);
 
 cudaError_t launch_selftest_bounded_wait(uint64_t timeout_ns, uint32_t* d_flag,
                                          cudaStream_t stream);

@@ -105,6 +105,10 @@ std::string build_plan_host(const h3attn_doc* docs, int32_t n_docs, const h3attn
       for (int32_t r = b; r < e; r += kUnitRows) units.push_back(WorkUnit{r, b, e, h, 0, n_kv, -1, 0});
   }
   if (units.size() >= (size_t(1) << 30)) return "too many work units";
+  p.ktiles_host.clear();
+  for (int32_t d = 0; d < n_docs; ++d)
+    for (int32_t t = p.cu_host[d]; t < p.cu_host[d + 1]; t += kKeyTile)
+      p.ktiles_host.push_back(int2{t, std::min(t + kKeyTile, p.cu_host[d + 1])});
   build_segments(units, grid, p.units_host, p.merges_host, &p.n_parts);
   p.n_units = (int32_t)p.units_host.size();
   return "";

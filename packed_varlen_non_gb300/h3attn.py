@@ -56,6 +56,8 @@ _SIGS = {
                        c_float, c_void_p, c_void_p],
     "h3attn_forward_fused_q": [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_int64,
                                c_void_p, c_int64, c_float, c_float, c_void_p, c_void_p],
+    "h3attn_fp8_quantize": [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_void_p, c_void_p,
+                            c_void_p, c_void_p, c_void_p, c_void_p],
     "h3attn_forward_noalloc": [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_int64,
                                c_void_p, c_int64, c_float, c_void_p, c_void_p],
     "h3attn_get_device_error": [c_void_p, c_void_p],
@@ -221,6 +223,17 @@ def h3attn_forward_fused_q(plan, q_raw, k, v, o, gain_q, softmax_scale: float, e
                                          _ptr(o), _row_stride(o, o_row_stride), _ptr(gain_q),
                                          int(gain_head_stride), float(eps), float(softmax_scale), _ptr(lse),
                                          _stream(stream)), "h3attn_forward_fused_q")
+
+
+def h3attn_fp8_quantize(plan, q_hat, k_hat, v, q8, k8, v8t, sq, sk, sv, qkv_row_stride=None, stream=None):
+    """FP8 quantisation of q-hat, k-hat, v (see include/h3attn.h for layouts)."""
+    if qkv_row_stride is None and not isinstance(q_hat, int):
+        strides = {int(x.stride(0)) for x in (q_hat, k_hat, v)}
+        if len(strides) != 1:
+            raise ValueError(f"q, k and v must share one row stride (got {sorted(strides)})")
+    _check(load().h3attn_fp8_quantize(plan, _ptr(q_hat), _ptr(k_hat), _ptr(v), _row_stride(q_hat, qkv_row_stride),
+                                      _ptr(q8), _ptr(k8), _ptr(v8t), _ptr(sq), _ptr(sk), _ptr(sv), _stream(stream)),
+           "h3attn_fp8_quantize")
 
 
 def h3attn_forward_noalloc(cu_seqlens, num_heads: int, q, k, v, o, softmax_scale: float, lse=None,
