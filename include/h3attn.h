@@ -183,8 +183,10 @@ h3attn_status h3attn_forward_fused_q(h3attn_plan_t plan, const void* q_raw, cons
  *   k8  [S,H,128] e4m3, scale sk [H,S] per (head, 128-key tile of a document,
  *       i.e. tokens [a + 128j, min(a + 128j + 128, b)) of document [a, b)),
  *       stored for every token of the tile;
- *   v8t [H,128,S_pad] e4m3 (S_pad = S rounded up to 16; channel-major, keys
- *       contiguous), scale sv [H,128] per (head, channel) over all tokens.
+ *   v8t [H,128,V] e4m3, channel-major with keys contiguous; document d's
+ *       keys start at key sum_{d'<d} ceil(L_d'/16)*16 (a 16-key boundary, the
+ *       gaps zero), V = that sum over all documents (h3attn_plan_fp8_v_keys);
+ *       scale sv [H,128] per (head, channel) over all tokens.
  * scale = amax / 448 (1 for an all-zero row, tile or channel); code =
  * e4m3(x / scale), both divisions correctly rounded fp32, round to nearest
  * even with saturation to +-448.  All outputs are device buffers owned by the
@@ -193,6 +195,26 @@ h3attn_status h3attn_forward_fused_q(h3attn_plan_t plan, const void* q_raw, cons
 h3attn_status h3attn_fp8_quantize(h3attn_plan_t plan, const void* q_hat, const void* k_hat, const void* v,
                                   int64_t qkv_row_stride, void* q8, void* k8, void* v8t, float* sq, float* sk,
                                   float* sv, void* cuda_stream);
+
+/* Keys per row of the FP8 transposed V of this plan (see h3attn_fp8_quantize). */
+h3attn_status h3attn_plan_fp8_v_keys(h3attn_plan_t plan, int64_t* v_keys);
+
+/* The FP8 variant of h3attn_forward on h3attn_fp8_quantize's outputs: for
+ * each head and query i of document [a, b),
+ *     s_ij = softmax_scale * sq_i * sk_j * <q8_i, k8_j>   (fp32 accumulation)
+ *     o_i  = sum_j P_ij (v8_j * sv) / sum_j p_ij
+ * where p_ij = exp(s_ij - m) with the kernel's reference max m (at most 2^8
+ * below the row max, so p <= 2^8) and P_ij is p_ij rounded to e4m3 for the
+ * FP8 PV product; lse as h3attn_forward.  The result approximates exact
+ * attention on the dequantised inputs within 2^-4 sum_j w_ij |v~_jc| +
+ * 2^-10 sum_j |v~_jc| (+ bf16 rounding of o), w the exact softmax weights.
+ * q8, k8: [S,H,128] e4m3; v8t, sq, sk, sv as h3attn_fp8_quantize writes them;
+ * o: bf16 with o_row_stride, must not overlap the inputs; lse_out as
+ * h3attn_forward.  Errors: EINVAL for null/misaligned pointers, a bad stride,
+ * o overlapping an input, softmax_scale not finite or <= 0. */
+h3attn_status h3attn_forward_fp8(h3attn_plan_t plan, const void* q8, const void* k8, const void* v8t,
+                                 const float* sq, const float* sk, const float* sv, void* o, int64_t o_row_stride,
+                                 float softmax_scale, float* lse_out, void* cuda_stream);
 
 /* Allocation-free forward.  The pages have no counterpart: this entry point
  * exists for callers that may not allocate device memory -- code whose device

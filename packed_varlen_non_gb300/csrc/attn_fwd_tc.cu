@@ -79,19 +79,24 @@ constexpr int kQWarp = 10;
 constexpr int kTileRows = 128;
 constexpr int kSlots = 6;                              // ring slots (16 KB each)
 constexpr int kGroups = kSlots / 2;                    // key/value groups in flight
-constexpr uint32_t kQTileBytes = 128 * 128 * 2;        // 32 KB, two 16 KB halves
-constexpr uint32_t kQHalfBytes = kQTileBytes / 2;
-constexpr uint32_t kSlotBytes = 64 * 128 * 2;          // 16 KB
-constexpr uint32_t kKHalfBytes = kSlotBytes / 2;       // 64 keys x 64 dims
-constexpr uint32_t kSmemQ = 0;                         // 2 buffers x 2 query tiles
-constexpr uint32_t kSmemKV = 4 * kQTileBytes;          // kSlots slots
-constexpr uint32_t kSmemBar = kSmemKV + kSlots * kSlotBytes;
 // barriers: q_full[4] q_empty[4] q_ready[4] kv_full[G] kv_empty[G] s_ready[2] p_ready[2] o_ready[2] drain
 constexpr int kNumBars = 12 + 2 * kGroups + 2 + 2 + 2 + 1;
-constexpr uint32_t kSmemMisc = kSmemBar + kNumBars * 8;
-constexpr uint32_t kSmemBytes = kSmemMisc + 16;
-constexpr size_t kSmemAlloc = kSmemBytes + 1024;       // slack to align the base to 1 KB
-static_assert(kSmemAlloc <= 227 * 1024, "shared memory per CTA");
+// Shared-memory layout: 2 buffers x 2 query tiles, then the ring.  bf16: a Q
+// tile is 128 rows x 128 dims in two 16 KB halves of 64 dims, a slot 16 KB;
+// fp8 (e4m3): a Q tile is one 16 KB block of 128-byte rows, a slot 8 KB.
+template <bool kFp8>
+struct Cfg {
+  static constexpr uint32_t QTileBytes = kFp8 ? 128 * 128 : 128 * 128 * 2;
+  static constexpr uint32_t SlotBytes = kFp8 ? 64 * 128 : 64 * 128 * 2;
+  static constexpr uint32_t SmemQ = 0;
+  static constexpr uint32_t SmemKV = 4 * QTileBytes;
+  static constexpr uint32_t SmemBar = SmemKV + kSlots * SlotBytes;
+  static constexpr uint32_t SmemMisc = SmemBar + kNumBars * 8;
+  static constexpr size_t SmemAlloc = SmemMisc + 16 + 1024;  // slack to align the base to 1 KB
+  static_assert(SmemAlloc <= 227 * 1024, "shared memory per CTA");
+};
+constexpr uint32_t kQHalfBytes = 128 * 128;            // bf16 Q tile: one half (64 dims)
+constexpr uint32_t kKHalfBytes = 64 * 128;             // bf16 K half-tile: one half (64 dims)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint64_t kTimeoutNs = 2000000000ull;         // 2 s
 constexpr float kRescaleThreshold = 8.0f;              // log2 units: rescale when max grows by > 2^8
@@ -102,6 +107,8 @@ static_assert(kUnitRows == 4 * kTileRows, "a unit is two query tiles in each CTA
 constexpr uint32_t kIdescBase = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((256u >> 4) << 24);
 constexpr uint32_t kIdescQK = kIdescBase;              // A, B K-major
 constexpr uint32_t kIdescPV = kIdescBase | (1u << 16);  // B (V) MN-major
+// kind::f8f6f4: e4m3 A and B (type code 0), fp32 accumulator, M = 256, N = 128, both K-major
+constexpr uint32_t kIdescF8 = (1u << 4) | ((128u >> 3) << 17) | ((256u >> 4) << 24);
 
 // Q slot i = 2 * buffer + query tile; the unit with ordinal k (per pair) uses buffer k & 1.
 struct Bars {
@@ -119,6 +126,7 @@ struct Bars {
 
 struct UnitGeom {
   int32_t q0, kv0, kv1, head, lo, hi, part, n_st;  // key tiles [lo, hi)
+  int32_t v_off;                                   // FP8: the document's first key in the transposed V
 };
 
 __device__ __forceinline__ UnitGeom unit_geom(const WorkUnit* units, int u) {
@@ -132,22 +140,32 @@ __device__ __forceinline__ UnitGeom unit_geom(const WorkUnit* units, int u) {
   g.lo = x.x;
   g.hi = x.y;
   g.part = x.z;
+  g.v_off = x.w;
   g.n_st = (w.x + 2 * kTileRows < w.z) ? 2 : 1;  // query tile 1 of the pair holds rows from 256 on
   return g;
 }
 
-// This CTA's half of a K tile: keys [key0 + 64 rank, +64), all 128 dims (two boxes).
+// This CTA's half of a K tile: keys [key0 + 64 rank, +64), all 128 dims (bf16:
+// two boxes of 64 dims; fp8: one box of 128-byte rows).
+template <bool kFp8>
 __device__ __forceinline__ void load_k_half(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int head,
                                             int32_t key0, uint32_t rank, uint64_t pol) {
   const int32_t row = key0 + 64 * (int32_t)rank;
   dev::tma_load_2d(dst, tm, bar, head * 128, row, pol);
-  dev::tma_load_2d(dst + kKHalfBytes, tm, bar, head * 128 + 64, row, pol);
+  if constexpr (!kFp8) dev::tma_load_2d(dst + kKHalfBytes, tm, bar, head * 128 + 64, row, pol);
 }
 
-// This CTA's half of a V tile: 128 keys, dims [64 rank, 64 rank + 64) (one box).
+// This CTA's half of a V tile: 128 keys, dims [64 rank, 64 rank + 64) (one box;
+// fp8: rows of the transposed V, one per channel, 128 keys each).
+// key0: the tile's first key row (bf16) or its first key in the transposed V,
+// a multiple of 16 (fp8).
+template <bool kFp8>
 __device__ __forceinline__ void load_v_half(uint32_t dst, const CUtensorMap* tm, uint32_t bar, int head,
                                             int32_t key0, uint32_t rank, uint64_t pol) {
-  dev::tma_load_2d(dst, tm, bar, head * 128 + 64 * (int32_t)rank, key0, pol);
+  if constexpr (kFp8)
+    dev::tma_load_2d(dst, tm, bar, key0, head * 128 + 64 * (int32_t)rank, pol);
+  else
+    dev::tma_load_2d(dst, tm, bar, head * 128 + 64 * (int32_t)rank, key0, pol);
 }
 
 // Shared-memory descriptors, split into 32-bit words: the high word (stride
@@ -193,7 +211,7 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint3
 // 8 pair MMAs of K = 16 keys in one block.  Step kk reads P at TMEM column
 // +8 kk and V at +2 KB kk; the first accumulates only if acc.
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, bool acc) {
-  const uint32_t vb = desc_lo(v_smem, kSlotBytes);
+  const uint32_t vb = desc_lo(v_smem, Cfg<false>::SlotBytes);
   asm volatile(
       "{\n\t.reg .pred p0, p1;\n\t.reg .b64 b;\n\t.reg .b32 t, y;\n\t"
       "setp.ne.u32 p0, %4, 0;\n\t"
@@ -218,6 +236,53 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
       : "memory");
 }
 
+// FP8: S = Q (e4m3, 128-byte rows) * K^T (e4m3, 64 keys per CTA), 4 pair MMAs
+// of K = 32 (32 bytes of each row per step).
+__device__ __forceinline__ void issue_qk_f8(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+  const uint32_t qa = desc_lo(q_smem, 16), kb = desc_lo(k_smem, 16);
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 a, b;\n\t.reg .b32 x, y;\n\t"
+      "setp.ne.u32 p0, %4, %4;\n\t"
+      "setp.eq.u32 p1, %4, %4;\n\t"
+      "mov.b64 a, {%1, %3};\n\tmov.b64 b, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], a, b, %5, p0;\n\t"
+      "add.u32 x, %1, 2;\n\tadd.u32 y, %2, 2;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], a, b, %5, p1;\n\t"
+      "add.u32 x, %1, 4;\n\tadd.u32 y, %2, 4;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], a, b, %5, p1;\n\t"
+      "add.u32 x, %1, 6;\n\tadd.u32 y, %2, 6;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], a, b, %5, p1;\n\t}" ::"r"(d_tmem),
+      "r"(qa), "r"(kb), "r"(kDescHi), "r"(0u), "r"(kIdescF8)
+      : "memory");
+}
+
+// FP8: O (+)= P (TMEM, e4m3, four per column) * V (e4m3, K-major: 64 channels
+// per CTA, 128-byte rows of keys), 4 pair MMAs of K = 32 keys.
+__device__ __forceinline__ void issue_pv_f8(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, bool acc) {
+  const uint32_t vb = desc_lo(v_smem, 16);
+  asm volatile(
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 b;\n\t.reg .b32 t, y;\n\t"
+      "setp.ne.u32 p0, %4, 0;\n\t"
+      "setp.eq.u32 p1, %4, %4;\n\t"
+      "mov.b64 b, {%2, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], [%1], b, %5, p0;\n\t"
+      "add.u32 t, %1, 8;\n\tadd.u32 y, %2, 2;\n\tmov.b64 b, {y, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], [t], b, %5, p1;\n\t"
+      "add.u32 t, %1, 16;\n\tadd.u32 y, %2, 4;\n\tmov.b64 b, {y, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], [t], b, %5, p1;\n\t"
+      "add.u32 t, %1, 24;\n\tadd.u32 y, %2, 6;\n\tmov.b64 b, {y, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], [t], b, %5, p1;\n\t}" ::"r"(d_tmem),
+      "r"(p_tmem), "r"(vb), "r"(kDescHi), "r"(acc ? 1u : 0u), "r"(kIdescF8)
+      : "memory");
+}
+
+// two e4m3 codes of fp32 values (lo in the low byte), round to nearest even, saturating
+__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
 // One query row's 128 scores from TMEM (4 loads of 32 columns); keys past
 // the document end (column >= rem) are set to -inf.
 __device__ __forceinline__ void load_scores(uint32_t t_s, uint32_t (&r)[4][32], int rem) {
@@ -228,6 +293,18 @@ __device__ __forceinline__ void load_scores(uint32_t t_s, uint32_t (&r)[4][32], 
 #pragma unroll
     for (int c = 0; c < 128; ++c)
       if (c >= rem) r[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+  }
+}
+
+// fp8: 32 accumulator columns times their V channel scales (fp32).
+__device__ __forceinline__ void scale_by_channel(uint32_t (&ov)[32], const float* sv) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float4 s4 = __ldg(reinterpret_cast<const float4*>(sv) + i);
+    ov[4 * i] = __float_as_uint(__uint_as_float(ov[4 * i]) * s4.x);
+    ov[4 * i + 1] = __float_as_uint(__uint_as_float(ov[4 * i + 1]) * s4.y);
+    ov[4 * i + 2] = __float_as_uint(__uint_as_float(ov[4 * i + 2]) * s4.z);
+    ov[4 * i + 3] = __float_as_uint(__uint_as_float(ov[4 * i + 3]) * s4.w);
   }
 }
 
@@ -306,16 +383,21 @@ static __device__ __noinline__ void norm_rope_q_row(uint32_t tile, uint32_t r, c
   }
 }
 
+// kFp8: the FP8 variant -- e4m3 Q, K, V (V transposed, keys contiguous) with
+// scales (per query row, per key tile, per V channel), kind::f8f6f4 MMAs,
+// P rounded to e4m3; everything else as the bf16 kernel.
+template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, ForwardArgs a) {
+  using C = Cfg<kFp8>;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = dev::smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   unsigned char* smem = smem_raw + (sbase - raw);
-  const Bars bars{sbase + kSmemBar};
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kSmemMisc);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kSmemMisc + 4);
+  const Bars bars{sbase + C::SmemBar};
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::SmemMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::SmemMisc + 4);
 
   const uint32_t warp = dev::warp_id_uniform();
   const uint32_t lane = threadIdx.x & 31;
@@ -373,11 +455,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const int i = 2 * (k & 1) + s;
           ok = dev::mbar_wait(bars.q_empty(i), (q_use[i] & 1) ^ 1, abort_flag, a.err, kTimeoutNs);
           if (!ok) break;
-          const uint32_t dst = sbase + kSmemQ + i * kQTileBytes;
-          dev::mbar_arrive_expect_tx(bars.q_full(i), kQTileBytes);
+          const uint32_t dst = sbase + C::SmemQ + i * C::QTileBytes;
+          dev::mbar_arrive_expect_tx(bars.q_full(i), C::QTileBytes);
           const int32_t row = g.q0 + s * 2 * kTileRows + (int32_t)rank * kTileRows;
           dev::tma_load_2d(dst, &tm_q, bars.q_full(i), g.head * 128, row, pol_q);
-          dev::tma_load_2d(dst + kQHalfBytes, &tm_q, bars.q_full(i), g.head * 128 + 64, row, pol_q);
+          if constexpr (!kFp8)
+            dev::tma_load_2d(dst + kQHalfBytes, &tm_q, bars.q_full(i), g.head * 128 + 64, row, pol_q);
           ++q_use[i];
         }
       };
@@ -394,8 +477,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (!ok) break;
           ok = dev::mbar_wait(bars.kv_empty(0), 1, abort_flag, a.err, kTimeoutNs);
           if (!ok) break;
-          dev::mbar_arrive_expect_tx(bars.kv_full(0), kSlotBytes);
-          load_k_half(sbase + kSmemKV, &tm_k, bars.kv_full(0), g.head, g.kv0 + g.lo * kTileRows, rank, pol_kv);
+          dev::mbar_arrive_expect_tx(bars.kv_full(0), C::SlotBytes);
+          load_k_half<kFp8>(sbase + C::SmemKV, &tm_k, bars.kv_full(0), g.head, g.kv0 + g.lo * kTileRows, rank,
+                            pol_kv);
           grp = 1;
         }
         for (int j = g.lo; ok && j < g.hi; ++j) {
@@ -411,12 +495,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t b = grp % kGroups;
           ok = dev::mbar_wait(bars.kv_empty(b), ((grp / kGroups) & 1) ^ 1, abort_flag, a.err, kTimeoutNs);
           if (!ok) break;
-          dev::mbar_arrive_expect_tx(bars.kv_full(b), has_k ? 2 * kSlotBytes : kSlotBytes);
-          load_v_half(sbase + kSmemKV + ((2 * grp - 1) % kSlots) * kSlotBytes, &tm_v, bars.kv_full(b), g.head,
-                      g.kv0 + j * kTileRows, rank, pol_kv);
+          dev::mbar_arrive_expect_tx(bars.kv_full(b), has_k ? 2 * C::SlotBytes : C::SlotBytes);
+          load_v_half<kFp8>(sbase + C::SmemKV + ((2 * grp - 1) % kSlots) * C::SlotBytes, &tm_v, bars.kv_full(b),
+                            g.head, (kFp8 ? g.v_off : g.kv0) + j * kTileRows, rank, pol_kv);
           if (has_k)
-            load_k_half(sbase + kSmemKV + ((2 * grp) % kSlots) * kSlotBytes, &tm_k, bars.kv_full(b), k_head,
-                        k_row, rank, pol_kv);
+            load_k_half<kFp8>(sbase + C::SmemKV + ((2 * grp) % kSlots) * C::SlotBytes, &tm_k, bars.kv_full(b),
+                              k_head, k_row, rank, pol_kv);
           ++grp;
           // the next unit's Q tiles, behind this unit's first group
           if (j == g.lo && has_next) load_q(unit_geom(a.units, u + n_pairs), k + 1);
@@ -465,7 +549,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
           if (s >= g.n_st) break;
-          issue_qk(tmem + s * 128, sbase + kSmemQ + (qb + s) * kQTileBytes, sbase + kSmemKV + k0 * kSlotBytes);
+          if constexpr (kFp8)
+            issue_qk_f8(tmem + s * 128, sbase + C::SmemQ + (qb + s) * C::QTileBytes,
+                        sbase + C::SmemKV + k0 * C::SlotBytes);
+          else
+            issue_qk(tmem + s * 128, sbase + C::SmemQ + (qb + s) * C::QTileBytes,
+                     sbase + C::SmemKV + k0 * C::SlotBytes);
           dev::mma_commit_pair_mc(bars.s_ready(s), kPairMask);
           if (g.hi - g.lo == 1) dev::mma_commit_pair_mc(bars.q_empty(qb + s), kPairMask);
         }
@@ -483,10 +572,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             if (!ok) break;
             ++p_it;
             dev::tc_fence_after();
-            issue_pv(tmem + 256 + s * 128, tmem + s * 128, sbase + kSmemKV + vslot * kSlotBytes, j > g.lo);
+            if constexpr (kFp8)
+              issue_pv_f8(tmem + 256 + s * 128, tmem + s * 128, sbase + C::SmemKV + vslot * C::SlotBytes, j > g.lo);
+            else
+              issue_pv(tmem + 256 + s * 128, tmem + s * 128, sbase + C::SmemKV + vslot * C::SlotBytes, j > g.lo);
             if (more) {
-              issue_qk(tmem + s * 128, sbase + kSmemQ + (qb + s) * kQTileBytes,
-                       sbase + kSmemKV + kslot * kSlotBytes);
+              if constexpr (kFp8)
+                issue_qk_f8(tmem + s * 128, sbase + C::SmemQ + (qb + s) * C::QTileBytes,
+                            sbase + C::SmemKV + kslot * C::SlotBytes);
+              else
+                issue_qk(tmem + s * 128, sbase + C::SmemQ + (qb + s) * C::QTileBytes,
+                         sbase + C::SmemKV + kslot * C::SlotBytes);
               dev::mma_commit_pair_mc(bars.s_ready(s), kPairMask);
               if (j + 2 == g.hi) dev::mma_commit_pair_mc(bars.q_empty(qb + s), kPairMask);
             } else {
@@ -520,14 +616,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int i = 2 * (k & 1) + s;
         bool good = dev::mbar_wait(bars.q_full(i), q_use[i] & 1, abort_flag, a.err, kTimeoutNs);
         ++q_use[i];
-        if (good && fuse_q) {
+        if (!kFp8 && good && fuse_q) {
           const int32_t row0 = g.q0 + s * 2 * kTileRows + (int32_t)rank * kTileRows;
           const float* gain = a.gain_q + (int64_t)g.head * a.gain_head_stride;
 #pragma unroll 1
           for (uint32_t r = lane; r < (uint32_t)kTileRows; r += 32) {
             const int32_t row = row0 + (int32_t)r;
             if (row < g.kv1)
-              norm_rope_q_row(sbase + kSmemQ + i * kQTileBytes, r, gain, a.rope + (int64_t)row * kRopeHalf, a.eps);
+              norm_rope_q_row(sbase + C::SmemQ + i * C::QTileBytes, r, gain, a.rope + (int64_t)row * kRopeHalf, a.eps);
           }
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the tensor cores
         }
@@ -562,8 +658,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const bool releases = lead_lane && st == g.n_st - 1;
       const bool checks_kv = lead_lane && st == 0;
       float m_used = -INFINITY, l = 0.f;
+      // fp8: this row's q scale (1 for rows past the tensor, never stored)
+      float sq_row = 1.f;
+      if constexpr (kFp8) {
+        const int32_t row = g.q0 + st * 2 * kTileRows + (int32_t)rank * kTileRows + (int32_t)row_in_tile;
+        if (row < a.S) sq_row = __ldg(a.sq + (int64_t)g.head * a.S + row);
+      }
       for (int j = g.lo; j < g.hi; ++j) {
         const uint32_t t = t_unit + (j - g.lo);  // the pair's running key-tile count
+        // score scale in log2 units: softmax_scale log2(e), times the q-row and
+        // key-tile scales for fp8
+        float rsc = sl2;
+        if constexpr (kFp8) rsc = sl2 * sq_row * __ldg(a.sk + (int64_t)g.head * a.S + g.kv0 + j * kTileRows);
         ok = dev::mbar_wait(bars.s_ready(st), s_it & 1, abort_flag, a.err, kTimeoutNs);
         if (!ok) break;
         ++s_it;
@@ -585,7 +691,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 8; ++i) mx[i] = dev::max3(mx[i], sv[c + i], sv[c + 8 + i]);
         const float m_new =
-            dev::max3(dev::max3(mx[0], mx[1], mx[2]), dev::max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * sl2;
+            dev::max3(dev::max3(mx[0], mx[1], mx[2]), dev::max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * rsc;
         // The reference max only moves when the row max grows by more than
         // 2^8 (then O and l are rescaled; the final O / l is unchanged).  The
         // O row is rescaled after P is written: the next PV waits for p_ready.
@@ -603,13 +709,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int c = 0; c < 32; ++c) {
             // packed pair arithmetic: one f32x2 FMA for the exponents, one f32x2 add for the sums
             float x0, x1;
-            dev::fma2(x0, x1, sv[64 * h + 2 * c], sv[64 * h + 2 * c + 1], sl2, sl2, neg, neg);
+            dev::fma2(x0, x1, sv[64 * h + 2 * c], sv[64 * h + 2 * c + 1], rsc, rsc, neg, neg);
             const float p0 = dev::ex2_approx(x0), p1 = dev::ex2_approx(x1);
             const int ai = 2 * (c & 3);
             dev::add2(rs8[ai], rs8[ai + 1], rs8[ai], rs8[ai + 1], p0, p1);
-            p[c] = dev::pack_bf16x2(p0, p1);
+            if constexpr (kFp8) {
+              // e4m3, four per column (p <= 2^8 < 448: no scale)
+              const uint32_t two = e4m3x2(p0, p1);
+              p[c >> 1] = (c & 1) ? (p[c >> 1] | (two << 16)) : two;
+            } else {
+              p[c] = dev::pack_bf16x2(p0, p1);
+            }
           }
-          dev::tmem_st32(t_s + 32 * h, p);
+          if constexpr (kFp8) {
+            uint32_t p16[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) p16[i] = p[i];
+            dev::tmem_st16(t_s + 16 * h, p16);
+          } else {
+            dev::tmem_st32(t_s + 32 * h, p);
+          }
         }
         const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
         l = l * alpha + rs;
@@ -659,6 +778,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           uint32_t ov[32];
           dev::tmem_ld32(t_o + c * 32, ov);
           dev::tmem_wait_ld();
+          if constexpr (kFp8) scale_by_channel(ov, a.sv + g.head * kHeadDim + c * 32);
           if (valid) {
 #pragma unroll
             for (int e = 0; e < 8; ++e)
@@ -676,6 +796,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t ov[32];
         dev::tmem_ld32(t_o + c * 32, ov);
         dev::tmem_wait_ld();
+        if constexpr (kFp8) scale_by_channel(ov, a.sv + g.head * kHeadDim + c * 32);
         if (valid) {
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -752,20 +873,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-bool make_map(CUtensorMap* m, const void* base, int64_t S, int32_t H, int64_t stride, uint32_t box_rows,
-              std::string* why) {
+// 2D tensor map, 128-byte swizzle: inner extent `inner` elements of `esize`
+// bytes (the tile box is 128 bytes wide), `outer` rows `row_bytes` apart.
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType type, uint32_t esize, uint64_t inner,
+              uint64_t outer, uint64_t row_bytes, uint32_t box_rows, std::string* why) {
   auto fn = encode_fn();
   if (fn == nullptr) {
     if (why) *why = "cuTensorMapEncodeTiled is unavailable";
     return false;
   }
-  cuuint64_t dims[2] = {(cuuint64_t)H * kHeadDim, (cuuint64_t)S};
-  cuuint64_t strides[1] = {(cuuint64_t)stride * 2};
-  cuuint32_t box[2] = {64, box_rows};
+  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+  cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+  cuuint32_t box[2] = {128 / esize, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = fn(m, type, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     if (why) *why = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string((int)r);
     return false;
@@ -773,11 +895,41 @@ bool make_map(CUtensorMap* m, const void* base, int64_t S, int32_t H, int64_t st
   return true;
 }
 
+template <bool kFp8>
+cudaError_t set_smem_attr() {
+  static std::once_flag once;
+  static cudaError_t attr = cudaSuccess;
+  std::call_once(once, [] {
+    attr = cudaFuncSetAttribute(attn_fwd_tc_kernel<kFp8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)Cfg<kFp8>::SmemAlloc);
+  });
+  return attr;
+}
+
+template <bool kFp8>
+cudaError_t launch_pairs(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const ForwardArgs& a,
+                         int device, int num_sms, cudaStream_t stream, std::string* why) {
+  cudaError_t e = set_smem_attr<kFp8>();
+  if (e != cudaSuccess) {
+    if (why) *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
+    return e;
+  }
+  const int slots = forward_slots(device, num_sms);
+  const int pairs = a.n_units < slots ? a.n_units : slots;
+  attn_fwd_tc_kernel<kFp8><<<2 * pairs, kThreads, Cfg<kFp8>::SmemAlloc, stream>>>(mq, mk, mv, a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || a.n_merges == 0) return e;
+  const int64_t warps = (int64_t)a.n_merges * kUnitRows;
+  attn_merge_kernel<<<(int)((warps + 7) / 8), 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 int forward_slots(int device, int num_sms) {
   // Concurrent CTA pairs: the occupancy of the pair cluster (one CTA per SM),
-  // asked once per device; half the SMs if the query fails.
+  // asked once per device; half the SMs if the query fails.  The FP8 kernel
+  // has the same threads and registers and less shared memory.
   static int slots[64];
   static std::once_flag once[64];
   if (device < 0 || device >= 64) return num_sms / 2 > 0 ? num_sms / 2 : 1;
@@ -786,18 +938,16 @@ int forward_slots(int device, int num_sms) {
     int prev = -1;
     cudaGetDevice(&prev);
     if (prev != device) cudaSetDevice(device);
-    if (cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc) ==
-        cudaSuccess) {
+    if (set_smem_attr<false>() == cudaSuccess) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(2 * (num_sms / 2 > 0 ? num_sms / 2 : 1));
       cfg.blockDim = dim3(kThreads);
-      cfg.dynamicSmemBytes = kSmemAlloc;
-      if (cudaOccupancyMaxActiveClusters(&n, attn_fwd_tc_kernel, &cfg) != cudaSuccess) n = 0;
+      cfg.dynamicSmemBytes = Cfg<false>::SmemAlloc;
+      if (cudaOccupancyMaxActiveClusters(&n, attn_fwd_tc_kernel<false>, &cfg) != cudaSuccess) n = 0;
     }
     cudaGetLastError();
     if (prev != device && prev >= 0) cudaSetDevice(prev);
     slots[device] = n > 0 ? n : (num_sms / 2 > 0 ? num_sms / 2 : 1);
-    fprintf(stderr, "[probe] max active clusters %d, slots %d\n", n, slots[device]);
   });
   return slots[device];
 }
@@ -805,27 +955,26 @@ int forward_slots(int device, int num_sms) {
 cudaError_t launch_forward(const ForwardArgs& a, int device, int num_sms, cudaStream_t stream, std::string* why) {
   if (a.n_units == 0) return cudaSuccess;
   CUtensorMap mq, mk, mv;
-  if (!make_map(&mq, a.q, a.S, a.H, a.qkv_stride, kTileRows, why) ||
-      !make_map(&mk, a.k, a.S, a.H, a.qkv_stride, kTileRows / 2, why) ||
-      !make_map(&mv, a.v, a.S, a.H, a.qkv_stride, kTileRows, why))
+  const uint64_t inner = (uint64_t)a.H * kHeadDim, row = (uint64_t)a.qkv_stride * 2;
+  if (!make_map(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, a.S, row, kTileRows, why) ||
+      !make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, a.S, row, kTileRows / 2, why) ||
+      !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, a.S, row, kTileRows, why))
     return cudaErrorInvalidValue;
-  static std::once_flag once;
-  static cudaError_t attr = cudaSuccess;
-  std::call_once(once, [] {
-    attr = cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemAlloc);
-  });
-  if (attr != cudaSuccess) {
-    if (why) *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
-    return attr;
-  }
-  const int slots = forward_slots(device, num_sms);
-  const int pairs = a.n_units < slots ? a.n_units : slots;
-  attn_fwd_tc_kernel<<<2 * pairs, kThreads, kSmemAlloc, stream>>>(mq, mk, mv, a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || a.n_merges == 0) return e;
-  const int64_t warps = (int64_t)a.n_merges * kUnitRows;
-  attn_merge_kernel<<<(int)((warps + 7) / 8), 256, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pairs<false>(mq, mk, mv, a, device, num_sms, stream, why);
+}
+
+cudaError_t launch_forward_fp8(const ForwardArgs& a, int device, int num_sms, cudaStream_t stream,
+                               std::string* why) {
+  if (a.n_units == 0) return cudaSuccess;
+  CUtensorMap mq, mk, mv;
+  const uint64_t inner = (uint64_t)a.H * kHeadDim;  // bytes per token row of q8 / k8
+  if (!make_map(&mq, a.q, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, inner, a.S, inner, kTileRows, why) ||
+      !make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, inner, a.S, inner, kTileRows / 2, why) ||
+      // transposed V: H * 128 channel rows of S keys, v_row_bytes apart
+      !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.v_row_bytes, inner, a.v_row_bytes, kTileRows / 2,
+                why))
+    return cudaErrorInvalidValue;
+  return launch_pairs<true>(mq, mk, mv, a, device, num_sms, stream, why);
 }
 
 }  // namespace h3

@@ -169,7 +169,7 @@ h3attn_status h3attn_plan_create(const h3attn_doc* docs, int32_t n_docs,
       (e = cudaMalloc(&p->d_rope, n_rope * sizeof(float2))) != cudaSuccess ||
       (e = cudaMalloc(&p->d_units, p->units_host.size() * sizeof(WorkUnit))) != cudaSuccess ||
       (e = cudaMalloc(&p->d_err, 16)) != cudaSuccess ||
-      (e = cudaMalloc(&p->d_ktiles, p->ktiles_host.size() * sizeof(int2))) != cudaSuccess ||
+      (e = cudaMalloc(&p->d_ktiles, p->ktiles_host.size() * sizeof(int4))) != cudaSuccess ||
       (p->n_parts > 0 &&
        ((e = cudaMalloc(&p->d_merges, p->merges_host.size() * sizeof(MergeUnit))) != cudaSuccess ||
         (e = cudaMalloc(&p->d_part_o, (size_t)p->n_parts * kUnitRows * kHeadDim * sizeof(float))) != cudaSuccess ||
@@ -189,7 +189,7 @@ h3attn_status h3attn_plan_create(const h3attn_doc* docs, int32_t n_docs,
        (e = cudaMemcpyAsync(p->d_merges, p->merges_host.data(), p->merges_host.size() * sizeof(MergeUnit),
                             cudaMemcpyHostToDevice, st)) != cudaSuccess) ||
       (e = cudaMemsetAsync(p->d_err, 0, 16, st)) != cudaSuccess ||
-      (e = cudaMemcpyAsync(p->d_ktiles, p->ktiles_host.data(), p->ktiles_host.size() * sizeof(int2),
+      (e = cudaMemcpyAsync(p->d_ktiles, p->ktiles_host.data(), p->ktiles_host.size() * sizeof(int4),
                            cudaMemcpyHostToDevice, st)) != cudaSuccess ||
       (e = cudaStreamSynchronize(st)) != cudaSuccess) {
     free_plan_device(p);
@@ -381,7 +381,7 @@ h3attn_status h3attn_fp8_quantize(h3attn_plan_t plan, const void* q_hat, const v
     return fail(H3ATTN_EINVAL, "row stride must be >= H*128 = %lld and a multiple of 8", (long long)width);
   const int64_t S = plan->S;
   const int32_t H = plan->num_heads;
-  const int64_t s_pad = (S + 15) / 16 * 16;
+  const int64_t v_pad = plan->v_pad;
   // outputs must not share bytes with the inputs or with each other
   const uintptr_t in_lo[3] = {reinterpret_cast<uintptr_t>(q_hat), reinterpret_cast<uintptr_t>(k_hat),
                               reinterpret_cast<uintptr_t>(v)};
@@ -389,7 +389,7 @@ h3attn_status h3attn_fp8_quantize(h3attn_plan_t plan, const void* q_hat, const v
   const uintptr_t out_lo[6] = {reinterpret_cast<uintptr_t>(q8), reinterpret_cast<uintptr_t>(k8),
                                reinterpret_cast<uintptr_t>(v8t), reinterpret_cast<uintptr_t>(sq),
                                reinterpret_cast<uintptr_t>(sk), reinterpret_cast<uintptr_t>(sv)};
-  const uintptr_t out_len[6] = {(uintptr_t)(S * width), (uintptr_t)(S * width), (uintptr_t)(H * kHeadDim * s_pad),
+  const uintptr_t out_len[6] = {(uintptr_t)(S * width), (uintptr_t)(S * width), (uintptr_t)(H * kHeadDim * v_pad),
                                 (uintptr_t)(H * S * 4), (uintptr_t)(H * S * 4), (uintptr_t)(H * kHeadDim * 4)};
   for (int o = 0; o < 6; ++o) {
     for (int i = 0; i < 3; ++i)
@@ -403,9 +403,62 @@ h3attn_status h3attn_fp8_quantize(h3attn_plan_t plan, const void* q_hat, const v
   cudaError_t e = g.enter(plan->device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
   Fp8QuantArgs a{q_hat, k_hat, v, qkv_row_stride, S, H, plan->d_ktiles, (int32_t)plan->ktiles_host.size(),
-                 q8, k8, v8t, s_pad, sq, sk, sv};
+                 q8, k8, v8t, v_pad, sq, sk, sv};
   e = launch_fp8_quantize(a, plan->num_sms, static_cast<cudaStream_t>(cuda_stream));
   return e == cudaSuccess ? H3ATTN_OK : cuda_fail(e, "fp8 quantise launch");
+}
+
+h3attn_status h3attn_plan_fp8_v_keys(h3attn_plan_t plan, int64_t* v_keys) {
+  clear_error();
+  if (h3attn_status s = check_plan(plan)) return s;
+  if (!v_keys) return fail(H3ATTN_EINVAL, "NULL output pointer");
+  *v_keys = plan->v_pad;
+  return H3ATTN_OK;
+}
+
+h3attn_status h3attn_forward_fp8(h3attn_plan_t plan, const void* q8, const void* k8, const void* v8t,
+                                 const float* sq, const float* sk, const float* sv, void* o, int64_t o_row_stride,
+                                 float softmax_scale, float* lse_out, void* cuda_stream) {
+  clear_error();
+  if (h3attn_status s = check_plan(plan)) return s;
+  if (!q8 || !k8 || !v8t || !sq || !sk || !sv || !o) return fail(H3ATTN_EINVAL, "NULL tensor or scale pointer");
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8t) || !aligned16(sq) || !aligned16(sk) || !aligned16(sv) ||
+      !aligned16(o))
+    return fail(H3ATTN_EINVAL, "tensors and scales must be 16-byte aligned");
+  if (lse_out && (reinterpret_cast<uintptr_t>(lse_out) & 3u))
+    return fail(H3ATTN_EINVAL, "lse_out must be 4-byte aligned");
+  const int64_t width = (int64_t)plan->num_heads * kHeadDim;
+  if (o_row_stride < width || (o_row_stride % 8))
+    return fail(H3ATTN_EINVAL, "o_row_stride must be >= H*128 = %lld and a multiple of 8", (long long)width);
+  if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f))
+    return fail(H3ATTN_EINVAL, "softmax_scale must be finite and > 0");
+  const int64_t S = plan->S;
+  const int32_t H = plan->num_heads;
+  const Extent eo = extent_of(o, S, H, o_row_stride);
+  const uintptr_t in_lo[3] = {reinterpret_cast<uintptr_t>(q8), reinterpret_cast<uintptr_t>(k8),
+                              reinterpret_cast<uintptr_t>(v8t)};
+  const uintptr_t in_len[3] = {(uintptr_t)(S * width), (uintptr_t)(S * width),
+                               (uintptr_t)(H * kHeadDim * plan->v_pad)};
+  for (int i = 0; i < 3; ++i)
+    if (in_lo[i] < eo.hi && eo.lo < in_lo[i] + in_len[i]) return fail(H3ATTN_EINVAL, "o overlaps an input");
+  if (lse_out) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(lse_out), hi = lo + (uintptr_t)S * H * 4;
+    if (!(hi <= eo.lo || eo.hi <= lo)) return fail(H3ATTN_EINVAL, "lse_out overlaps o");
+  }
+  DeviceGuard g;
+  cudaError_t e = g.enter(plan->device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+  ForwardArgs a{q8, k8, v8t, o, lse_out, width, o_row_stride, S, H,
+                softmax_scale * 1.4426950408889634f, plan->d_units, plan->n_units, plan->d_err,
+                plan->d_merges, (int32_t)plan->merges_host.size(), plan->d_part_o, plan->d_part_ml,
+                nullptr, 0, 0.f, nullptr, sq, sk, sv, plan->v_pad};
+  std::string why;
+  e = launch_forward_fp8(a, plan->device, plan->num_sms, static_cast<cudaStream_t>(cuda_stream), &why);
+  if (e != cudaSuccess) {
+    if (!why.empty()) return fail(H3ATTN_ECUDA, "forward: %s", why.c_str());
+    return cuda_fail(e, "forward launch");
+  }
+  return H3ATTN_OK;
 }
 
 h3attn_status h3attn_get_device_error(h3attn_plan_t plan, void* cuda_stream) {

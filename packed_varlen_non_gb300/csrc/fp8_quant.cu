@@ -1,7 +1,9 @@
 // Quantisation of the attention inputs to FP8 (e4m3) for the FP8 variant of
 // the forward: q-hat per (token, head) row, k-hat per (head, 128-key tile of a
 // document), v per (head, channel) over all tokens and written transposed
-// (channel-major, keys contiguous) for the PV product's K-major B operand.
+// (channel-major, keys contiguous, each document starting on a 16-key
+// boundary so that a key tile's TMA coordinate is 16-byte aligned) for the PV
+// product's K-major B operand.
 //
 // Pages: vllm.cpp PR #26 "feat(minimax-h3)" and the "h3-spark" model card,
 // "What this config does" name a SageAttention2++-style INT8/FP8 attention
@@ -75,7 +77,7 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(Fp8QuantArgs a) {
 __global__ void __launch_bounds__(256) quant_ktiles_kernel(Fp8QuantArgs a) {
   __shared__ float warp_max[8];
   const int tile = blockIdx.x, h = blockIdx.y;
-  const int2 te = a.tiles[tile];
+  const int4 te = a.tiles[tile];
   const int64_t t = te.x + (threadIdx.x >> 1);
   const bool live = t < te.y;
   const int d0 = (threadIdx.x & 1) * 64;
@@ -130,20 +132,23 @@ __global__ void __launch_bounds__(256) vmax_kernel(Fp8QuantArgs a) {
   }
 }
 
-// v, pass 2: codes, transposed through shared memory: one block per (head,
-// 128-token chunk) writes v8t[h][c][t0 .. t0 + 128) for all 128 channels.
+// v, pass 2: codes, transposed through shared memory: one block per (key
+// tile, head) writes v8t[h][c][vb .. vb + n) for all 128 channels, where the
+// tile's n <= 128 keys start at vb in the transposed layout (every document
+// starts on a 16-key boundary); a document's last tile also zero-fills up to
+// the next boundary.
 __global__ void __launch_bounds__(256) vquant_kernel(Fp8QuantArgs a) {
   __shared__ __align__(16) uint8_t tile[128][128 + 16];
+  const int4 te = a.tiles[blockIdx.x];
   const int h = blockIdx.y;
-  const int64_t t0 = (int64_t)blockIdx.x * 128;
+  const int n = te.y - te.x;
   const int tl = threadIdx.x >> 1, c0 = (threadIdx.x & 1) * 64;
-  const int64_t t = t0 + tl;
   const uint32_t* bits = reinterpret_cast<const uint32_t*>(a.sv);
-  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.v) + t * a.stride + h * kHeadDim + c0;
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.v) + (int64_t)(te.x + tl) * a.stride + h * kHeadDim + c0;
 #pragma unroll 1
   for (int c = 0; c < 64; c += 8) {
     float f[8];
-    if (t < a.S) {
+    if (tl < n) {
       unpack8(__ldg(reinterpret_cast<const uint4*>(x + c)), f);
     } else {
 #pragma unroll
@@ -159,12 +164,13 @@ __global__ void __launch_bounds__(256) vquant_kernel(Fp8QuantArgs a) {
     }
   }
   __syncthreads();
-  // thread i writes channel i/2, tokens [64 (i%2), +64) as four 16-byte pieces
+  // thread i writes channel i/2, keys [64 (i%2), +64) as 16-byte pieces
   const int ch = threadIdx.x >> 1, k0 = (threadIdx.x & 1) * 64;
-  uint8_t* out = static_cast<uint8_t*>(a.v8t) + ((int64_t)h * kHeadDim + ch) * a.s_pad + t0 + k0;
+  const int n16 = (n + 15) / 16 * 16;
+  uint8_t* out = static_cast<uint8_t*>(a.v8t) + ((int64_t)h * kHeadDim + ch) * a.v_pad + te.z + k0;
 #pragma unroll
   for (int p = 0; p < 4; ++p)
-    if (t0 + k0 + p * 16 < a.s_pad)
+    if (k0 + p * 16 < n16)
       *reinterpret_cast<uint4*>(out + p * 16) = *reinterpret_cast<const uint4*>(&tile[ch][k0 + p * 16]);
 }
 
@@ -185,7 +191,7 @@ cudaError_t launch_fp8_quantize(const Fp8QuantArgs& a, int num_sms, cudaStream_t
   cudaError_t e = cudaMemsetAsync(a.sv, 0, (size_t)a.H * kHeadDim * sizeof(float), stream);
   if (e != cudaSuccess) return e;
   vmax_kernel<<<(int)((a.S + kVmaxTokens - 1) / kVmaxTokens), 256, 0, stream>>>(a);
-  vquant_kernel<<<dim3((unsigned)((a.S + 127) / 128), a.H), 256, 0, stream>>>(a);
+  vquant_kernel<<<dim3(a.n_tiles, a.H), 256, 0, stream>>>(a);
   vscale_kernel<<<(a.H * kHeadDim + 255) / 256, 256, 0, stream>>>(a);
   return cudaGetLastError();
 }

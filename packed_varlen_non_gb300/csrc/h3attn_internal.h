@@ -38,7 +38,7 @@ struct WorkUnit {
   int32_t tile_lo;
   int32_t tile_hi;
   int32_t part;
-  int32_t pad;
+  int32_t v_off;   // the document's first key in the FP8 transposed V (16-key aligned)
 };
 static_assert(sizeof(WorkUnit) == 32, "WorkUnit is read as two 16-byte vectors");
 
@@ -74,7 +74,10 @@ struct Plan {
   std::vector<WorkUnit> units_host;  // segment list (see build_segments)
   std::vector<MergeUnit> merges_host;
   int32_t n_parts = 0;
-  std::vector<int2> ktiles_host;     // (begin, end) of every document's 128-key tiles
+  // every document's 128-key tiles: (begin, end, first key in the FP8
+  // transposed V, 0); that V gives each document a 16-key aligned start
+  std::vector<int4> ktiles_host;
+  int64_t v_pad = 0;                 // keys per row of the FP8 transposed V
 
   int32_t* d_cu = nullptr;
   float2* d_rope = nullptr;          // [S, 48] (cos, sin)
@@ -84,7 +87,7 @@ struct Plan {
   float* d_part_o = nullptr;         // [n_parts, kUnitRows, 128] unnormalised O
   float2* d_part_ml = nullptr;       // [n_parts, kUnitRows] (running max in log2 units, sum)
   uint32_t* d_err = nullptr;         // device error word
-  int2* d_ktiles = nullptr;
+  int4* d_ktiles = nullptr;
 };
 
 // Host-side plan construction (plan.cpp); returns an empty string or an error.
@@ -139,12 +142,19 @@ struct ForwardArgs {
   int64_t gain_head_stride;
   float eps;
   const float2* rope;          // [S, 48] (cos, sin)
+  // FP8 variant (h3attn_forward_fp8): scales of the e4m3 inputs
+  const float* sq;             // [H, S]
+  const float* sk;             // [H, S]
+  const float* sv;             // [H, 128]
+  int64_t v_row_bytes;         // row stride of the transposed V (the plan's v_pad)
 };
 // Work slots of the forward: CTA pairs that run at the same time on `device`
 // (the plan's segment list is balanced for this many).
 int forward_slots(int device, int num_sms);
 cudaError_t launch_forward(const ForwardArgs& a, int device, int num_sms, cudaStream_t stream,
                            std::string* why);
+cudaError_t launch_forward_fp8(const ForwardArgs& a, int device, int num_sms, cudaStream_t stream,
+                               std::string* why);
 
 // FP8 (e4m3) quantisation of q-hat, k-hat and v (fp8_quant.cu).
 struct Fp8QuantArgs {
@@ -154,12 +164,12 @@ struct Fp8QuantArgs {
   int64_t stride;              // row stride of q-hat, k-hat, v (elements)
   int64_t S;
   int32_t H;
-  const int2* tiles;           // (begin, end) of every document's 128-key tiles
+  const int4* tiles;           // (begin, end, V key, 0) of every document's 128-key tiles
   int32_t n_tiles;
   void* q8;                    // [S, H, 128] codes
   void* k8;                    // [S, H, 128] codes
-  void* v8t;                   // [H, 128, s_pad] codes, keys contiguous
-  int64_t s_pad;               // S rounded up to a multiple of 16
+  void* v8t;                   // [H, 128, v_pad] codes, keys contiguous, documents 16-key aligned
+  int64_t v_pad;
   float* sq;                   // [H, S]
   float* sk;                   // [H, S] (each token carries its tile's scale)
   float* sv;                   // [H, 128]

@@ -97,18 +97,27 @@ std::string build_plan_host(const h3attn_doc* docs, int32_t n_docs, const h3attn
   std::stable_sort(order.begin(), order.end(), [&](int32_t a, int32_t b) {
     return (p.cu_host[a + 1] - p.cu_host[a]) > (p.cu_host[b + 1] - p.cu_host[b]);
   });
+  // FP8 transposed V: document d's keys start at v_off[d], a multiple of 16
+  std::vector<int32_t> v_off(n_docs);
+  int64_t v_pad = 0;
+  for (int32_t d = 0; d < n_docs; ++d) {
+    v_off[d] = (int32_t)v_pad;
+    v_pad += (p.cu_host[d + 1] - p.cu_host[d] + 15) / 16 * 16;
+  }
+  if (v_pad >= (int64_t(1) << 31)) return "too many tokens";
+  p.v_pad = v_pad;
   std::vector<WorkUnit> units;
   for (int32_t d : order) {
     const int32_t b = p.cu_host[d], e = p.cu_host[d + 1];
     const int32_t n_kv = (e - b + kKeyTile - 1) / kKeyTile;
     for (int32_t h = 0; h < opts.num_heads; ++h)
-      for (int32_t r = b; r < e; r += kUnitRows) units.push_back(WorkUnit{r, b, e, h, 0, n_kv, -1, 0});
+      for (int32_t r = b; r < e; r += kUnitRows) units.push_back(WorkUnit{r, b, e, h, 0, n_kv, -1, v_off[d]});
   }
   if (units.size() >= (size_t(1) << 30)) return "too many work units";
   p.ktiles_host.clear();
   for (int32_t d = 0; d < n_docs; ++d)
     for (int32_t t = p.cu_host[d]; t < p.cu_host[d + 1]; t += kKeyTile)
-      p.ktiles_host.push_back(int2{t, std::min(t + kKeyTile, p.cu_host[d + 1])});
+      p.ktiles_host.push_back(int4{t, std::min(t + kKeyTile, p.cu_host[d + 1]), v_off[d] + (t - p.cu_host[d]), 0});
   build_segments(units, grid, p.units_host, p.merges_host, &p.n_parts);
   p.n_units = (int32_t)p.units_host.size();
   return "";

@@ -58,6 +58,9 @@ _SIGS = {
                                c_void_p, c_int64, c_float, c_float, c_void_p, c_void_p],
     "h3attn_fp8_quantize": [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_void_p, c_void_p,
                             c_void_p, c_void_p, c_void_p, c_void_p],
+    "h3attn_plan_fp8_v_keys": [c_void_p, POINTER(c_int64)],
+    "h3attn_forward_fp8": [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
+                           c_int64, c_float, c_void_p, c_void_p],
     "h3attn_forward_noalloc": [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_int64,
                                c_void_p, c_int64, c_float, c_void_p, c_void_p],
     "h3attn_get_device_error": [c_void_p, c_void_p],
@@ -234,6 +237,19 @@ def h3attn_fp8_quantize(plan, q_hat, k_hat, v, q8, k8, v8t, sq, sk, sv, qkv_row_
     _check(load().h3attn_fp8_quantize(plan, _ptr(q_hat), _ptr(k_hat), _ptr(v), _row_stride(q_hat, qkv_row_stride),
                                       _ptr(q8), _ptr(k8), _ptr(v8t), _ptr(sq), _ptr(sk), _ptr(sv), _stream(stream)),
            "h3attn_fp8_quantize")
+
+
+def h3attn_plan_fp8_v_keys(plan) -> int:
+    n = c_int64()
+    _check(load().h3attn_plan_fp8_v_keys(plan, ctypes.byref(n)), "h3attn_plan_fp8_v_keys")
+    return n.value
+
+
+def h3attn_forward_fp8(plan, q8, k8, v8t, sq, sk, sv, o, softmax_scale: float, lse=None, o_row_stride=None,
+                       stream=None):
+    _check(load().h3attn_forward_fp8(plan, _ptr(q8), _ptr(k8), _ptr(v8t), _ptr(sq), _ptr(sk), _ptr(sv), _ptr(o),
+                                     _row_stride(o, o_row_stride), float(softmax_scale), _ptr(lse),
+                                     _stream(stream)), "h3attn_forward_fp8")
 
 
 def h3attn_forward_noalloc(cu_seqlens, num_heads: int, q, k, v, o, softmax_scale: float, lse=None,

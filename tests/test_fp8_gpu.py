@@ -15,12 +15,17 @@ from tests.gpu_cases import docs_1d, random_tensors
 pytestmark = pytest.mark.gpu
 
 
-def fp8_buffers(S, Hh):
+def v_offsets(lens):
+    """first key of every document in the transposed V (16-key aligned starts)"""
+    pads = [(L + 15) // 16 * 16 for L in lens]
+    return np.concatenate([[0], np.cumsum(pads)])
+
+
+def fp8_buffers(S, Hh, v_keys):
     dev = torch.device("cuda")
-    s_pad = (S + 15) // 16 * 16
     return dict(q8=torch.empty(S, Hh * 128, dtype=torch.uint8, device=dev),
                 k8=torch.empty(S, Hh * 128, dtype=torch.uint8, device=dev),
-                v8t=torch.empty(Hh, 128, s_pad, dtype=torch.uint8, device=dev),
+                v8t=torch.full((Hh, 128, v_keys), 0x7F, dtype=torch.uint8, device=dev),  # NaN codes: gaps must be written
                 sq=torch.empty(Hh, S, dtype=torch.float32, device=dev),
                 sk=torch.empty(Hh, S, dtype=torch.float32, device=dev),
                 sv=torch.empty(Hh, 128, dtype=torch.float32, device=dev))
@@ -31,17 +36,18 @@ def run_quantize(plan, S, Hh, q_bits, k_bits, v_bits):
     q = bf16_to_torch(q_bits).view(S, W)
     k = bf16_to_torch(k_bits).view(S, W)
     v = bf16_to_torch(v_bits).view(S, W)
-    b = fp8_buffers(S, Hh)
+    b = fp8_buffers(S, Hh, H.h3attn_plan_fp8_v_keys(plan.handle))
     H.h3attn_fp8_quantize(plan.handle, q, k, v, b["q8"], b["k8"], b["v8t"], b["sq"], b["sk"], b["sv"])
     torch.cuda.synchronize()
-    return {n: t.cpu().numpy() for n, t in b.items()}
+    return {n: t.cpu().numpy() for n, t in b.items()}, b
 
 
 def check_quantize(lens, Hh, t, what):
     S = sum(lens)
     cu = np.concatenate([[0], np.cumsum(lens)])
     with H.Plan(docs_1d(lens), Hh) as plan:
-        g = run_quantize(plan, S, Hh, t.q, t.k, t.v)
+        assert H.h3attn_plan_fp8_v_keys(plan.handle) == v_offsets(lens)[-1]
+        g, _ = run_quantize(plan, S, Hh, t.q, t.k, t.v)
     q8, sq, k8, sk, v8, sv = ofp8.quantize(synth.bf16_bits_to_f64(t.q), synth.bf16_bits_to_f64(t.k),
                                           synth.bf16_bits_to_f64(t.v), cu)
     assert np.array_equal(g["sq"], sq), f"{what}: q scales"
@@ -49,7 +55,12 @@ def check_quantize(lens, Hh, t, what):
     assert np.array_equal(g["sk"], sk), f"{what}: k scales"
     assert np.array_equal(g["k8"].reshape(S, Hh, 128), k8), f"{what}: k codes"
     assert np.array_equal(g["sv"], sv), f"{what}: v scales"
-    assert np.array_equal(g["v8t"][:, :, :S], v8.transpose(1, 2, 0)), f"{what}: v codes (transposed)"
+    vo = v_offsets(lens)
+    for d, L in enumerate(lens):
+        a = int(cu[d])
+        seg = g["v8t"][:, :, vo[d]:vo[d + 1]]
+        assert np.array_equal(seg[:, :, :L], v8[a:a + L].transpose(1, 2, 0)), f"{what}: v codes, doc {d}"
+        assert not seg[:, :, L:].any(), f"{what}: v gap after doc {d} not zero"
 
 
 @pytest.mark.parametrize("lens,Hh", [([1000, 3, 513, 129, 1], 3), ([255, 256, 257], 2), ([4096], 4)])
@@ -74,3 +85,65 @@ def test_quantize_workload_grid(lib):
     w = synth.config(2)
     t = synth.make_tensors(w)
     check_quantize(list(w.doc_lengths), w.num_heads, t, "config 2")
+
+
+def run_fp8(lens, Hh, t, scale=None):
+    """prologue (bf16) -> FP8 quantisation -> FP8 forward; returns the GPU
+    output, its lse, and the quantised inputs (host)"""
+    S = sum(lens)
+    W = Hh * 128
+    scale = 1.0 / np.sqrt(128.0) if scale is None else scale
+    dev = torch.device("cuda")
+    with H.Plan(docs_1d(lens), Hh) as plan:
+        q = bf16_to_torch(t.q).view(S, W)
+        k = bf16_to_torch(t.k).view(S, W)
+        v = bf16_to_torch(t.v).view(S, W)
+        qh, kh = torch.empty_like(q), torch.empty_like(k)
+        H.h3attn_qk_prologue(plan.handle, q, k, qh, kh, torch.from_numpy(t.gain_q).to(dev),
+                             torch.from_numpy(t.gain_k).to(dev), 1e-6)
+        b = fp8_buffers(S, Hh, H.h3attn_plan_fp8_v_keys(plan.handle))
+        H.h3attn_fp8_quantize(plan.handle, qh, kh, v, b["q8"], b["k8"], b["v8t"], b["sq"], b["sk"], b["sv"])
+        o = torch.full((S, W), float("nan"), dtype=torch.bfloat16, device=dev)
+        lse = torch.full((Hh, S), float("nan"), dtype=torch.float32, device=dev)
+        H.h3attn_forward_fp8(plan.handle, b["q8"], b["k8"], b["v8t"], b["sq"], b["sk"], b["sv"], o, scale, lse)
+        H.h3attn_get_device_error(plan.handle)
+        host = {n: x.cpu().numpy() for n, x in b.items()}
+        return (o.double().cpu().numpy().reshape(S, Hh, 128), lse.cpu().numpy(),
+                qh.double().cpu().numpy().reshape(S, Hh, 128), kh.double().cpu().numpy().reshape(S, Hh, 128), host)
+
+
+def check_fp8_forward(lens, Hh, t, rows=None, what=""):
+    from oracle import attention as oatt
+    S = sum(lens)
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    scale = 1.0 / np.sqrt(128.0)
+    o, lse, qh, kh, g = run_fp8(lens, Hh, t, scale)
+    # the quantised inputs are the oracle's (bit-exact), so the oracle's dequantised values serve
+    q8, sq, k8, sk, v8, sv = ofp8.quantize(qh, kh, synth.bf16_bits_to_f64(t.v), cu)
+    assert np.array_equal(g["q8"].reshape(S, Hh, 128), q8) and np.array_equal(g["sk"], sk)
+    qd, kd, vd = ofp8.dequantize(q8, sq, k8, sk, v8, sv)
+    rows = np.arange(S) if rows is None else rows
+    o_ref, lse_ref = oatt.attention_rows(qd[rows], kd, vd, cu, scale, range(Hh), rows)
+    bound = ofp8.error_bound(qd, kd, vd, cu, scale, range(Hh), rows)
+    tol = bound + 2.0 ** -8 * np.abs(o_ref) + 1e-4
+    err = np.abs(o[rows] - o_ref)
+    assert np.all(np.isfinite(o[rows])), f"{what}: non-finite output"
+    worst = float((err / tol).max())
+    assert worst <= 1.0, f"{what}: error {err.max():.3e} exceeds the P-rounding bound (ratio {worst:.2f})"
+    assert float(np.abs(lse[:, rows] - lse_ref).max()) <= 1e-3, f"{what}: lse"
+    return float(err.max()), float(err.mean())
+
+
+@pytest.mark.parametrize("lens,Hh", [([1000, 3, 513, 129, 1], 3), ([255, 256, 257, 700], 2)])
+def test_fp8_forward_within_bound(lib, lens, Hh):
+    t = random_tensors(sum(lens), Hh, seed=17 + len(lens))
+    check_fp8_forward(lens, Hh, t, what=str(lens))
+
+
+def test_fp8_forward_ref2va_sampled(lib):
+    from tests.gpu_cases import sample_rows
+    w = synth.config(3)
+    t = synth.make_tensors(w)
+    cu = np.concatenate([[0], np.cumsum(w.doc_lengths)])
+    rows = sample_rows(cu, per_edge=8, interior=24, seed=3)
+    check_fp8_forward(list(w.doc_lengths), w.num_heads, t, rows=rows, what="Ref2VA sampled")
