@@ -14,9 +14,10 @@ the plainest scheme that uses sm_103's FP8 tensor cores for both products:
            s_k = amax over the tile's tokens and dims / 448
     v:     one scale per (head, channel) over all S tokens
            s_v = amax_t |v| / 448
-    code = e4m3(x / s) with x / s one fp32 division (round to nearest even)
-    and e4m3 round-to-nearest-even with saturation to +-448; an all-zero
-    row, tile or channel takes s = 1.
+    code = e4m3(x * r) with r = 448 / amax (one fp32 division per row, tile
+    or channel), x * r one fp32 product (round to nearest even), and e4m3
+    round-to-nearest-even with saturation to +-448; an all-zero row, tile or
+    channel takes s = r = 1.  Dequantisation multiplies the code by s.
   the attention it approximates: exact softmax attention (two-pass, fp64) on
     the dequantised values q~ = code_q s_q, k~ = code_k s_k, v~ = code_v s_v.
     The kernel additionally rounds the probabilities P to e4m3 for the PV
@@ -79,13 +80,23 @@ def e4m3_encode(y: np.ndarray) -> np.ndarray:
 
 
 def _scale(amax: np.ndarray) -> np.ndarray:
+    """dequantisation scale s = amax / 448 (fp32; 1 for amax = 0)"""
     amax = np.asarray(amax, dtype=np.float32)
-    s = amax / np.float32(E4M3_MAX)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        s = amax / np.float32(E4M3_MAX)
     return np.where(amax > 0, s, np.float32(1.0)).astype(np.float32)
 
 
-def _codes(x: np.ndarray, s: np.ndarray) -> np.ndarray:
-    y = np.asarray(x, dtype=np.float32) / np.asarray(s, dtype=np.float32)  # one fp32 division
+def _recip(amax: np.ndarray) -> np.ndarray:
+    """quantisation factor r = 448 / amax (fp32; 1 for amax = 0)"""
+    amax = np.asarray(amax, dtype=np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        r = np.float32(E4M3_MAX) / amax
+    return np.where(amax > 0, r, np.float32(1.0)).astype(np.float32)
+
+
+def _codes(x: np.ndarray, r: np.ndarray) -> np.ndarray:
+    y = np.asarray(x, dtype=np.float32) * np.asarray(r, dtype=np.float32)  # one fp32 product
     return e4m3_encode(y.astype(np.float32))
 
 
@@ -93,8 +104,8 @@ def quantize_rows(x: np.ndarray):
     """Per (token, head) rows.  x: [S, H, D] (values of bf16).  Returns
     codes [S, H, D] uint8 and scales [H, S] fp32."""
     x = np.asarray(x, dtype=np.float32)
-    s = _scale(np.abs(x).max(axis=2))               # [S, H]
-    return _codes(x, s[:, :, None]), np.ascontiguousarray(s.T)
+    amax = np.abs(x).max(axis=2)                     # [S, H]
+    return _codes(x, _recip(amax)[:, :, None]), np.ascontiguousarray(_scale(amax).T)
 
 
 def key_tiles(cu: np.ndarray, tile: int = 128):
@@ -115,9 +126,9 @@ def quantize_key_tiles(x: np.ndarray, cu: np.ndarray):
     codes = np.zeros((S, H, D), dtype=np.uint8)
     scales = np.zeros((H, S), dtype=np.float32)
     for a, b in key_tiles(cu):
-        s = _scale(np.abs(x[a:b]).max(axis=(0, 2)))  # [H]
-        codes[a:b] = _codes(x[a:b], s[None, :, None])
-        scales[:, a:b] = s[:, None]
+        amax = np.abs(x[a:b]).max(axis=(0, 2))       # [H]
+        codes[a:b] = _codes(x[a:b], _recip(amax)[None, :, None])
+        scales[:, a:b] = _scale(amax)[:, None]
     return codes, scales
 
 
@@ -125,8 +136,8 @@ def quantize_channels(x: np.ndarray):
     """Per (head, channel) over all tokens.  Returns codes [S, H, D] uint8 and
     scales [H, D] fp32."""
     x = np.asarray(x, dtype=np.float32)
-    s = _scale(np.abs(x).max(axis=0))                # [H, D]
-    return _codes(x, s[None, :, :]), s
+    amax = np.abs(x).max(axis=0)                     # [H, D]
+    return _codes(x, _recip(amax)[None, :, :]), _scale(amax)
 
 
 def quantize(q_hat: np.ndarray, k_hat: np.ndarray, v: np.ndarray, cu: np.ndarray):

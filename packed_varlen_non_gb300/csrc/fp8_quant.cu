@@ -8,11 +8,11 @@
 // Pages: vllm.cpp PR #26 "feat(minimax-h3)" and the "h3-spark" model card,
 // "What this config does" name a SageAttention2++-style INT8/FP8 attention
 // without its scheme; this is the plainest scheme that runs both products on
-// FP8 tensor cores.  Every decision is made in fp32 -- scale = amax / 448 by
-// one correctly rounded division (1 for an all-zero row, tile or channel),
-// code = e4m3(x / scale) by one correctly rounded division and the hardware
-// round-to-nearest-even conversion with saturation -- so the codes are the
-// ones an fp32 reference computes.
+// FP8 tensor cores.  Every decision is made in fp32 -- scale = amax / 448 and
+// r = 448 / amax by correctly rounded divisions (both 1 for an all-zero row,
+// tile or channel), code = e4m3(x * r) by one correctly rounded product and
+// the hardware round-to-nearest-even conversion with saturation -- so the
+// codes are the ones an fp32 reference computes.
 #include <cuda_bf16.h>
 
 #include "device_common.cuh"
@@ -24,6 +24,7 @@ namespace {
 constexpr float kE4m3Max = 448.0f;
 
 __device__ __forceinline__ float fp8_scale(float amax) { return amax > 0.f ? __fdiv_rn(amax, kE4m3Max) : 1.f; }
+__device__ __forceinline__ float fp8_recip(float amax) { return amax > 0.f ? __fdiv_rn(kE4m3Max, amax) : 1.f; }
 
 // two e4m3 codes, lo in the low byte
 __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
@@ -42,10 +43,10 @@ __device__ __forceinline__ void unpack8(const uint4& raw, float (&x)[8]) {
 }
 
 // 8 codes (one lane's 8 dims) as 8 bytes
-__device__ __forceinline__ uint2 codes8(const float (&x)[8], float s) {
+__device__ __forceinline__ uint2 codes8(const float (&x)[8], float r) {
   uint32_t c[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) c[i] = e4m3x2(__fdiv_rn(x[2 * i], s), __fdiv_rn(x[2 * i + 1], s));
+  for (int i = 0; i < 4; ++i) c[i] = e4m3x2(__fmul_rn(x[2 * i], r), __fmul_rn(x[2 * i + 1], r));
   return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
 
@@ -66,9 +67,8 @@ __global__ void __launch_bounds__(256) quant_rows_kernel(Fp8QuantArgs a) {
     for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(f[e]));
 #pragma unroll
     for (int off = 8; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(mask, m, off, 16));
-    const float s = fp8_scale(m);
-    *reinterpret_cast<uint2*>(out + row * kHeadDim + lane16 * 8) = codes8(f, s);
-    if (lane16 == 0) a.sq[(int64_t)h * a.S + t] = s;
+    *reinterpret_cast<uint2*>(out + row * kHeadDim + lane16 * 8) = codes8(f, fp8_recip(m));
+    if (lane16 == 0) a.sq[(int64_t)h * a.S + t] = fp8_scale(m);
   }
 }
 
@@ -102,34 +102,37 @@ __global__ void __launch_bounds__(256) quant_ktiles_kernel(Fp8QuantArgs a) {
   m = warp_max[0];
 #pragma unroll
   for (int w = 1; w < 8; ++w) m = fmaxf(m, warp_max[w]);
-  const float s = fp8_scale(m);
   if (!live) return;
+  const float r = fp8_recip(m);
   uint8_t* out = static_cast<uint8_t*>(a.k8) + (t * a.H + h) * kHeadDim + d0;
 #pragma unroll
-  for (int c = 0; c < 8; ++c) *reinterpret_cast<uint2*>(out + c * 8) = codes8(f[c], s);
-  if (d0 == 0) a.sk[(int64_t)h * a.S + t] = s;
+  for (int c = 0; c < 8; ++c) *reinterpret_cast<uint2*>(out + c * 8) = codes8(f[c], r);
+  if (d0 == 0) a.sk[(int64_t)h * a.S + t] = fp8_scale(m);
 }
 
 // v, pass 1: per-(head, channel) amax over all tokens into the scale buffer's
-// bits (non-negative floats order like their bit patterns).
-constexpr int kVmaxTokens = 256;
-__global__ void __launch_bounds__(256) vmax_kernel(Fp8QuantArgs a) {
-  const int64_t t0 = (int64_t)blockIdx.x * kVmaxTokens;
+// bits (non-negative floats order like their bit patterns).  Block (x, y):
+// 128 groups of 8 channels from group 128 x, tokens [128 y, 128 y + 128);
+// consecutive threads read consecutive 16 bytes of a token row.
+constexpr int kVmaxTokens = 128;
+__global__ void __launch_bounds__(128) vmax_kernel(Fp8QuantArgs a) {
+  const int g = blockIdx.x * 128 + threadIdx.x;  // group of 8 channels
+  if (g >= a.H * 16) return;
+  const int h = g >> 4, c0 = (g & 15) * 8;
+  const int64_t t0 = (int64_t)blockIdx.y * kVmaxTokens;
   const int64_t t1 = t0 + kVmaxTokens < a.S ? t0 + kVmaxTokens : a.S;
-  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.v);
-  uint32_t* bits = reinterpret_cast<uint32_t*>(a.sv);
-  for (int g = threadIdx.x; g < a.H * 16; g += blockDim.x) {  // groups of 8 channels
-    const int h = g >> 4, c0 = (g & 15) * 8;
-    float m[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int64_t t = t0; t < t1; ++t) {
-      float f[8];
-      unpack8(__ldg(reinterpret_cast<const uint4*>(x + t * a.stride + h * kHeadDim + c0)), f);
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.v) + h * kHeadDim + c0;
+  float m[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+  for (int64_t t = t0; t < t1; ++t) {
+    float f[8];
+    unpack8(__ldg(reinterpret_cast<const uint4*>(x + t * a.stride)), f);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) m[e] = fmaxf(m[e], fabsf(f[e]));
-    }
-#pragma unroll
-    for (int e = 0; e < 8; ++e) atomicMax(bits + h * kHeadDim + c0 + e, __float_as_uint(m[e]));
+    for (int e = 0; e < 8; ++e) m[e] = fmaxf(m[e], fabsf(f[e]));
   }
+  uint32_t* bits = reinterpret_cast<uint32_t*>(a.sv) + h * kHeadDim + c0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) atomicMax(bits + e, __float_as_uint(m[e]));
 }
 
 // v, pass 2: codes, transposed through shared memory: one block per (key
@@ -139,11 +142,14 @@ __global__ void __launch_bounds__(256) vmax_kernel(Fp8QuantArgs a) {
 // the next boundary.
 __global__ void __launch_bounds__(256) vquant_kernel(Fp8QuantArgs a) {
   __shared__ __align__(16) uint8_t tile[128][128 + 16];
+  __shared__ float rc[128];  // per-channel 448 / amax
   const int4 te = a.tiles[blockIdx.x];
   const int h = blockIdx.y;
   const int n = te.y - te.x;
   const int tl = threadIdx.x >> 1, c0 = (threadIdx.x & 1) * 64;
-  const uint32_t* bits = reinterpret_cast<const uint32_t*>(a.sv);
+  if (threadIdx.x < 128)
+    rc[threadIdx.x] = fp8_recip(__uint_as_float(reinterpret_cast<const uint32_t*>(a.sv)[h * kHeadDim + threadIdx.x]));
+  __syncthreads();
   const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.v) + (int64_t)(te.x + tl) * a.stride + h * kHeadDim + c0;
 #pragma unroll 1
   for (int c = 0; c < 64; c += 8) {
@@ -156,9 +162,7 @@ __global__ void __launch_bounds__(256) vquant_kernel(Fp8QuantArgs a) {
     }
 #pragma unroll
     for (int e = 0; e < 8; e += 2) {
-      const float s0 = fp8_scale(__uint_as_float(bits[h * kHeadDim + c0 + c + e]));
-      const float s1 = fp8_scale(__uint_as_float(bits[h * kHeadDim + c0 + c + e + 1]));
-      const uint32_t two = e4m3x2(__fdiv_rn(f[e], s0), __fdiv_rn(f[e + 1], s1));
+      const uint32_t two = e4m3x2(__fmul_rn(f[e], rc[c0 + c + e]), __fmul_rn(f[e + 1], rc[c0 + c + e + 1]));
       tile[c0 + c + e][tl] = (uint8_t)(two & 0xff);
       tile[c0 + c + e + 1][tl] = (uint8_t)(two >> 8);
     }
@@ -190,7 +194,8 @@ cudaError_t launch_fp8_quantize(const Fp8QuantArgs& a, int num_sms, cudaStream_t
   quant_ktiles_kernel<<<dim3(a.n_tiles, a.H), 256, 0, stream>>>(a);
   cudaError_t e = cudaMemsetAsync(a.sv, 0, (size_t)a.H * kHeadDim * sizeof(float), stream);
   if (e != cudaSuccess) return e;
-  vmax_kernel<<<(int)((a.S + kVmaxTokens - 1) / kVmaxTokens), 256, 0, stream>>>(a);
+  vmax_kernel<<<dim3((unsigned)((a.H * 16 + 127) / 128), (unsigned)((a.S + kVmaxTokens - 1) / kVmaxTokens)), 128, 0,
+                 stream>>>(a);
   vquant_kernel<<<dim3(a.n_tiles, a.H), 256, 0, stream>>>(a);
   vscale_kernel<<<(a.H * kHeadDim + 255) / 256, 256, 0, stream>>>(a);
   return cudaGetLastError();
