@@ -196,6 +196,10 @@ h3attn_status h3attn_fp8_quantize(h3attn_plan_t plan, const void* q_hat, const v
                                   int64_t qkv_row_stride, void* q8, void* k8, void* v8t, float* sq, float* sk,
                                   float* sv, void* cuda_stream);
 
+/* Kernels one h3attn_forward call launches with this plan: 1, or 2 when the
+ * last round of work units is split along the keys and merged. */
+h3attn_status h3attn_plan_forward_kernels(h3attn_plan_t plan, int32_t* n_kernels);
+
 /* Keys per row of the FP8 transposed V of this plan (see h3attn_fp8_quantize). */
 h3attn_status h3attn_plan_fp8_v_keys(h3attn_plan_t plan, int64_t* v_keys);
 

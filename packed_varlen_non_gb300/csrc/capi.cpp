@@ -408,6 +408,14 @@ h3attn_status h3attn_fp8_quantize(h3attn_plan_t plan, const void* q_hat, const v
   return e == cudaSuccess ? H3ATTN_OK : cuda_fail(e, "fp8 quantise launch");
 }
 
+h3attn_status h3attn_plan_forward_kernels(h3attn_plan_t plan, int32_t* n_kernels) {
+  clear_error();
+  if (h3attn_status s = check_plan(plan)) return s;
+  if (!n_kernels) return fail(H3ATTN_EINVAL, "NULL output pointer");
+  *n_kernels = plan->merges_host.empty() ? 1 : 2;
+  return H3ATTN_OK;
+}
+
 h3attn_status h3attn_plan_fp8_v_keys(h3attn_plan_t plan, int64_t* v_keys) {
   clear_error();
   if (h3attn_status s = check_plan(plan)) return s;

@@ -59,6 +59,7 @@ _SIGS = {
     "h3attn_fp8_quantize": [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_void_p, c_void_p,
                             c_void_p, c_void_p, c_void_p, c_void_p],
     "h3attn_plan_fp8_v_keys": [c_void_p, POINTER(c_int64)],
+    "h3attn_plan_forward_kernels": [c_void_p, POINTER(c_int32)],
     "h3attn_forward_fp8": [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                            c_int64, c_float, c_void_p, c_void_p],
     "h3attn_forward_noalloc": [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_int64,
@@ -237,6 +238,12 @@ def h3attn_fp8_quantize(plan, q_hat, k_hat, v, q8, k8, v8t, sq, sk, sv, qkv_row_
     _check(load().h3attn_fp8_quantize(plan, _ptr(q_hat), _ptr(k_hat), _ptr(v), _row_stride(q_hat, qkv_row_stride),
                                       _ptr(q8), _ptr(k8), _ptr(v8t), _ptr(sq), _ptr(sk), _ptr(sv), _stream(stream)),
            "h3attn_fp8_quantize")
+
+
+def h3attn_plan_forward_kernels(plan) -> int:
+    n = c_int32()
+    _check(load().h3attn_plan_forward_kernels(plan, ctypes.byref(n)), "h3attn_plan_forward_kernels")
+    return n.value
 
 
 def h3attn_plan_fp8_v_keys(plan) -> int:
