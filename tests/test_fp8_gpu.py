@@ -147,3 +147,30 @@ def test_fp8_forward_ref2va_sampled(lib):
     cu = np.concatenate([[0], np.cumsum(w.doc_lengths)])
     rows = sample_rows(cu, per_edge=8, interior=24, seed=3)
     check_fp8_forward(list(w.doc_lengths), w.num_heads, t, rows=rows, what="Ref2VA sampled")
+
+
+def test_fp8_rejects_bad_arguments(lib):
+    lens, Hh = [300, 40], 2
+    S = sum(lens)
+    dev = torch.device("cuda")
+    with H.Plan(docs_1d(lens), Hh) as plan:
+        vk = H.h3attn_plan_fp8_v_keys(plan.handle)
+        assert vk == 304 + 48
+        x = torch.zeros(S, Hh * 128, dtype=torch.bfloat16, device=dev)
+        b = fp8_buffers(S, Hh, vk)
+        args = [b["q8"], b["k8"], b["v8t"], b["sq"], b["sk"], b["sv"]]
+        # an output overlapping an input, two overlapping outputs, a misaligned scale pointer
+        for bad in ([x.view(torch.uint8)[:, :Hh * 128]] + args[1:], [args[0], args[0]] + args[2:],
+                    args[:3] + [b["sq"].view(-1)[1:]] + args[4:]):
+            with pytest.raises(H.H3AttnError) as e:
+                H.h3attn_fp8_quantize(plan.handle, x, x, x, *bad)
+            assert e.value.status == H.H3ATTN_EINVAL
+        o = torch.zeros(S, Hh * 128, dtype=torch.bfloat16, device=dev)
+        with pytest.raises(H.H3AttnError):
+            H.h3attn_forward_fp8(plan.handle, *args, o, float("nan"))
+        with pytest.raises(H.H3AttnError):  # o overlapping q8
+            H.h3attn_forward_fp8(plan.handle, *args, b["q8"].view(torch.bfloat16), 0.1)
+        H.h3attn_fp8_quantize(plan.handle, x, x, x, *args)  # valid calls still work
+        H.h3attn_forward_fp8(plan.handle, *args, o, 0.1)
+        H.h3attn_get_device_error(plan.handle)
+        assert H.h3attn_plan_forward_kernels(plan.handle) in (1, 2)
