@@ -192,10 +192,20 @@ def traffic_for_current_kernel():
         if ":" in line and not line.startswith("#"):
             key, val = line.split(":", 1)
             rec[key.strip()] = val.strip()
-    src = hashlib.sha256(open(FWD_SOURCE, "rb").read()).hexdigest()[:16]
-    if rec.get("kernel_source_sha256_16") != src:
+    if rec.get("kernel_code_sha256_16") != kernel_code_hash(FWD_SOURCE):
         return None
     return int(rec["dram_bytes_per_launch"])
+
+
+def kernel_code_hash(path: str) -> str:
+    """sha256[:16] of a CUDA source's code: // comments, trailing blanks and
+    empty lines removed, so that editing a comment keeps a profile valid."""
+    lines = []
+    for line in open(path, encoding="utf-8"):
+        code = line.split("//", 1)[0].rstrip() if not line.lstrip().startswith('"') else line.rstrip()
+        if code:
+            lines.append(code)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
 
 
 def max_over_ranks(ms: float, device) -> float:

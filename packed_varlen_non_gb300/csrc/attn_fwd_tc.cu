@@ -55,6 +55,14 @@
 // holding K(t) (everything before that QK has completed).  Q tiles: the even
 // CTA's "Q ready" barrier counts one arrival from the Q warp of each CTA.
 //
+// FP8 variant (template argument kFp8, h3attn_forward_fp8): the same kernel
+// on e4m3 Q, K and transposed V (channel rows of keys, every document
+// starting on a 16-key boundary) with fp32 scales -- kind::f8f6f4 pair MMAs of
+// K = 32, 16 KB Q tiles and 8 KB half-tiles in 128-byte rows, P rounded to
+// e4m3 and stored four per TMEM column (first 32 columns of S), the q-row x
+// key-tile scale folded into the softmax's score multiplier, the per-channel
+// V scale applied to O in the epilogue.
+//
 // Every mbarrier wait is bounded: on expiry the CTA raises an abort flag,
 // records a timeout in the device error word, drains its own copies and MMAs
 // with bounded waits, and leaves through the cluster barrier, where the pair
