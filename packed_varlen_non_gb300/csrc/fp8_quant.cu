@@ -50,50 +50,70 @@ __device__ __forceinline__ uint2 codes8(const float (&x)[8], float r) {
   return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
 
-// q-hat: 16 lanes per (token, head) row, 8 dims each.
+// q-hat: 16 lanes per (token, head) row, 8 dims each; four rows per lane
+// group per iteration, their loads issued together.
 __global__ void __launch_bounds__(256) quant_rows_kernel(Fp8QuantArgs a) {
   const int lane16 = threadIdx.x & 15;
   const unsigned mask = 0xffffu << (threadIdx.x & 16);
   const int64_t n_rows = a.S * a.H;
+  const int64_t stride = (int64_t)gridDim.x * 16;
   const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.q_hat);
   uint8_t* out = static_cast<uint8_t*>(a.q8);
-  for (int64_t row = (int64_t)blockIdx.x * 16 + (threadIdx.x >> 4); row < n_rows; row += (int64_t)gridDim.x * 16) {
-    const int64_t t = row / a.H;
-    const int h = (int)(row - t * a.H);
-    float f[8];
-    unpack8(__ldg(reinterpret_cast<const uint4*>(x + t * a.stride + h * kHeadDim + lane16 * 8)), f);
-    float m = 0.f;
+  for (int64_t row0 = (int64_t)blockIdx.x * 16 + (threadIdx.x >> 4); row0 < n_rows; row0 += 4 * stride) {
+    uint4 raw[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(f[e]));
+    for (int u = 0; u < 4; ++u) {
+      const int64_t row = row0 + u * stride;
+      if (row < n_rows) {
+        const int64_t t = row / a.H;
+        const int h = (int)(row - t * a.H);
+        raw[u] = __ldg(reinterpret_cast<const uint4*>(x + t * a.stride + h * kHeadDim + lane16 * 8));
+      } else {
+        raw[u] = make_uint4(0, 0, 0, 0);
+      }
+    }
 #pragma unroll
-    for (int off = 8; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(mask, m, off, 16));
-    *reinterpret_cast<uint2*>(out + row * kHeadDim + lane16 * 8) = codes8(f, fp8_recip(m));
-    if (lane16 == 0) a.sq[(int64_t)h * a.S + t] = fp8_scale(m);
+    for (int u = 0; u < 4; ++u) {
+      const int64_t row = row0 + u * stride;
+      if (row >= n_rows) break;  // uniform across the lane group
+      float f[8];
+      unpack8(raw[u], f);
+      float m = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(f[e]));
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(mask, m, off, 16));
+      *reinterpret_cast<uint2*>(out + row * kHeadDim + lane16 * 8) = codes8(f, fp8_recip(m));
+      if (lane16 == 0) {
+        const int64_t t = row / a.H;
+        a.sq[(int64_t)(row - t * a.H) * a.S + t] = fp8_scale(m);
+      }
+    }
   }
 }
 
-// k-hat: one block per (key tile, head); thread i takes token b + i/2, dims
-// [64 (i%2), +64).
+// k-hat: one block per (key tile, head); 16 lanes per token row (256
+// contiguous bytes), so thread i takes dims [8 (i%16), +8) of tokens
+// b + i/16, b + i/16 + 16, ... (eight of them).
 __global__ void __launch_bounds__(256) quant_ktiles_kernel(Fp8QuantArgs a) {
   __shared__ float warp_max[8];
   const int tile = blockIdx.x, h = blockIdx.y;
   const int4 te = a.tiles[tile];
-  const int64_t t = te.x + (threadIdx.x >> 1);
-  const bool live = t < te.y;
-  const int d0 = (threadIdx.x & 1) * 64;
-  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.k_hat) + t * a.stride + h * kHeadDim + d0;
+  const int tl0 = threadIdx.x >> 4, d0 = (threadIdx.x & 15) * 8;
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.k_hat) + h * kHeadDim + d0;
   float f[8][8];
   float m = 0.f;
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    if (live) {
-      unpack8(__ldg(reinterpret_cast<const uint4*>(x + c * 8)), f[c]);
+  for (int u = 0; u < 8; ++u) {
+    const int64_t t = te.x + tl0 + 16 * u;
+    if (t < te.y) {
+      unpack8(__ldg(reinterpret_cast<const uint4*>(x + t * a.stride)), f[u]);
     } else {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) f[c][e] = 0.f;
+      for (int e = 0; e < 8; ++e) f[u][e] = 0.f;
     }
 #pragma unroll
-    for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(f[c][e]));
+    for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(f[u][e]));
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
@@ -102,19 +122,23 @@ __global__ void __launch_bounds__(256) quant_ktiles_kernel(Fp8QuantArgs a) {
   m = warp_max[0];
 #pragma unroll
   for (int w = 1; w < 8; ++w) m = fmaxf(m, warp_max[w]);
-  if (!live) return;
-  const float r = fp8_recip(m);
-  uint8_t* out = static_cast<uint8_t*>(a.k8) + (t * a.H + h) * kHeadDim + d0;
+  const float r = fp8_recip(m), sc = fp8_scale(m);
+  uint8_t* out = static_cast<uint8_t*>(a.k8) + h * kHeadDim + d0;
 #pragma unroll
-  for (int c = 0; c < 8; ++c) *reinterpret_cast<uint2*>(out + c * 8) = codes8(f[c], r);
-  if (d0 == 0) a.sk[(int64_t)h * a.S + t] = fp8_scale(m);
+  for (int u = 0; u < 8; ++u) {
+    const int64_t t = te.x + tl0 + 16 * u;
+    if (t < te.y) {
+      *reinterpret_cast<uint2*>(out + t * a.H * kHeadDim) = codes8(f[u], r);
+      if (d0 == 0) a.sk[(int64_t)h * a.S + t] = sc;
+    }
+  }
 }
 
 // v, pass 1: per-(head, channel) amax over all tokens into the scale buffer's
 // bits (non-negative floats order like their bit patterns).  Block (x, y):
-// 128 groups of 8 channels from group 128 x, tokens [128 y, 128 y + 128);
+// 128 groups of 8 channels from group 128 x, tokens [64 y, 64 y + 64);
 // consecutive threads read consecutive 16 bytes of a token row.
-constexpr int kVmaxTokens = 128;
+constexpr int kVmaxTokens = 64;
 __global__ void __launch_bounds__(128) vmax_kernel(Fp8QuantArgs a) {
   const int g = blockIdx.x * 128 + threadIdx.x;  // group of 8 channels
   if (g >= a.H * 16) return;
@@ -123,7 +147,7 @@ __global__ void __launch_bounds__(128) vmax_kernel(Fp8QuantArgs a) {
   const int64_t t1 = t0 + kVmaxTokens < a.S ? t0 + kVmaxTokens : a.S;
   const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.v) + h * kHeadDim + c0;
   float m[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
+#pragma unroll 16
   for (int64_t t = t0; t < t1; ++t) {
     float f[8];
     unpack8(__ldg(reinterpret_cast<const uint4*>(x + t * a.stride)), f);
