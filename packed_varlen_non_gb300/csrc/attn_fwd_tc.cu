@@ -528,7 +528,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ----------------------------------------- MMA issuer (even CTA, pair) ----
     if (lane == 0 && rank == 0) {
-      uint32_t grp = 0, q_use[4] = {0, 0, 0, 0}, p_it0 = 0, p_it1 = 0;
+      // ring slots of the current group's V and K halves: group n uses slots
+      // 2n-1 and 2n (mod kSlots), advanced by two per key tile without a division
+      uint32_t vslot = 1, kslot = 2, q_use[4] = {0, 0, 0, 0}, p_it0 = 0, p_it1 = 0;
       bool ok = true;
       bool issued = false;
       int k = 0;
@@ -545,13 +547,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         // this unit's first K tile: group 0, or the K half of the previous
         // unit's last group (covered by that unit's last P-ready barrier)
-        uint32_t k0;
-        if (k == 0) {
-          k0 = 0;
-          grp = 1;
-        } else {
-          k0 = (2 * (grp - 1)) % kSlots;
-        }
+        const uint32_t k0 = k == 0 ? 0u : (kslot >= 2 ? kslot - 2 : kslot + kSlots - 2);
         if (!ok) break;
         dev::tc_fence_after();
 #pragma unroll
@@ -570,7 +566,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         for (int j = g.lo; j < g.hi; ++j) {
           // group grp = V(j) + the next K tile; its arrival in both CTAs is
           // implied by P-ready of query tile 0
-          const uint32_t vslot = (2 * grp - 1) % kSlots, kslot = (2 * grp) % kSlots;
           const bool more = j + 1 < g.hi;
 #pragma unroll
           for (int s = 0; s < 2; ++s) {
@@ -598,7 +593,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
           }
           if (!ok) break;
-          ++grp;
+          vslot = vslot + 2 >= (uint32_t)kSlots ? vslot + 2 - kSlots : vslot + 2;
+          kslot = kslot + 2 >= (uint32_t)kSlots ? kslot + 2 - kSlots : kslot + 2;
         }
       }
       if (!ok && issued) {
