@@ -680,6 +680,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // S of the last query tile is ready: every MMA before it is done, so
         // the group holding K(t) (and V(t-1)) is free in this CTA
         if (releases) dev::mbar_arrive(bars.kv_empty(t % kGroups));
+        // fp8 (whose per-tile softmax loop sets the period): test, without
+        // blocking, whether the next K/V group has landed; the blocking wait
+        // below then only runs if it had not
+        uint32_t kv_bar = 0, kv_par = 0;
+        bool kv_landed = false;
+        if constexpr (kFp8) {
+          kv_bar = bars.kv_full((t + 1) % kGroups);
+          kv_par = ((t + 1) / kGroups) & 1;
+          kv_landed = checks_kv && dev::mbar_test_wait(kv_bar, kv_par);
+        }
         __syncwarp();  // lanes leave the wait separately; the TMEM loads are warp-collective
         dev::tc_fence_after();
         uint32_t r[4][32];
@@ -754,10 +764,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
         // the next PV reads V(t) and the QK after it K(t+1): group t+1 must have
         // landed in this CTA before query tile 0 reports P ready
-        if (checks_kv)
+        if constexpr (kFp8) {
+          if (checks_kv && !kv_landed) ok = dev::mbar_wait(kv_bar, kv_par, abort_flag, a.err, kTimeoutNs);
+        } else if (checks_kv) {
           ok = dev::mbar_wait(bars.kv_full((t + 1) % kGroups), ((t + 1) / kGroups) & 1, abort_flag, a.err,
                               kTimeoutNs);
-        if (lane == 0) dev::mbar_arrive_cluster(p_ready_remote);  // P (and O) of the warp's 32 rows
+        }
+        if (lane == 0) {  // P (and O) of the warp's 32 rows
+          if (kFp8 && rank == 0)
+            dev::mbar_arrive(bars.p_ready(st));  // the even CTA's own barrier, arrived on locally
+          else
+            dev::mbar_arrive_cluster(p_ready_remote);
+        }
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
