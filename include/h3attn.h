@@ -187,9 +187,10 @@ h3attn_status h3attn_forward_fused_q(h3attn_plan_t plan, const void* q_raw, cons
  *       keys start at key sum_{d'<d} ceil(L_d'/16)*16 (a 16-key boundary, the
  *       gaps zero), V = that sum over all documents (h3attn_plan_fp8_v_keys);
  *       scale sv [H,128] per (head, channel) over all tokens.
- * scale = amax / 448 (1 for an all-zero row, tile or channel); code =
- * e4m3(x / scale), both divisions correctly rounded fp32, round to nearest
- * even with saturation to +-448.  All outputs are device buffers owned by the
+ * scale = amax / 448 and r = 448 / amax (both 1 for an all-zero row, tile or
+ * channel), each one correctly rounded fp32 division; code = e4m3(x * r), one
+ * correctly rounded fp32 product, then round to nearest even with saturation
+ * to +-448.  All outputs are device buffers owned by the
  * caller, 16-byte aligned, not overlapping the inputs or each other.
  * Errors: EINVAL for null/misaligned pointers, a bad stride, overlaps. */
 h3attn_status h3attn_fp8_quantize(h3attn_plan_t plan, const void* q_hat, const void* k_hat, const void* v,
@@ -199,6 +200,41 @@ h3attn_status h3attn_fp8_quantize(h3attn_plan_t plan, const void* q_hat, const v
 /* Kernels one h3attn_forward call launches with this plan: 1, or 2 when the
  * last round of work units is split along the keys and merged. */
 h3attn_status h3attn_plan_forward_kernels(h3attn_plan_t plan, int32_t* n_kernels);
+
+/* The forward's work list for a packed layout, built on the host alone (no
+ * device and no CUDA call is needed): the list h3attn_plan_create builds for
+ * n_pairs concurrent CTA pairs (a GB300 runs 76).  It schedules the
+ * per-document attention of h3attn_forward ([PR26] PR description: the
+ * cu_seqlens varlen contract) so that only tiles inside a document are ever
+ * visited, and places the work longest-processing-time first.
+ *
+ * A unit is up to 512 query rows of one head inside one document [b, e), over
+ * that document's 128-key tiles [tile_lo, tile_hi) (counted from b).  Units
+ * are listed longest document first, then head, then query rows; each is
+ * placed on the CTA pair with the least estimated load so far (ties to the
+ * lower pair), a segment's estimate being its key tiles plus one.  The units
+ * of the last partial round (U mod n_pairs of them, U the unit count) are
+ * split along their key tiles into about n_pairs pieces, which are placed the
+ * same way after the whole units; their partial results are merged by the
+ * forward.
+ *
+ * Outputs (host memory owned by the caller; pass units = NULL to get the
+ * sizes first):
+ *   *n_units       segments in the list;
+ *   *n_pairs_used  pairs with work (pairs 0 .. *n_pairs_used - 1; the others
+ *                  get none);
+ *   units          [*n_units][8] int32, grouped by pair: first query row, b,
+ *                  e, head, tile_lo, tile_hi, partial slot (-1: the segment
+ *                  writes the output itself), the document's first key in the
+ *                  FP8 transposed V;
+ *   unit_off       [*n_pairs_used + 1] int32: pair p runs units
+ *                  [unit_off[p], unit_off[p + 1]) in that order.
+ * units_cap is the capacity of units in segments.  Errors: EINVAL for a NULL
+ * cu_seqlens or output count, n_docs < 1, num_heads < 1, n_pairs outside
+ * [1, 1024], cu_seqlens[0] != 0, an empty document, or units_cap too small. */
+h3attn_status h3attn_work_list_host(const int32_t* cu_seqlens, int32_t n_docs, int32_t num_heads,
+                                    int32_t n_pairs, int32_t* units, int64_t units_cap, int32_t* unit_off,
+                                    int64_t* n_units, int32_t* n_pairs_used);
 
 /* Keys per row of the FP8 transposed V of this plan (see h3attn_fp8_quantize). */
 h3attn_status h3attn_plan_fp8_v_keys(h3attn_plan_t plan, int64_t* v_keys);
@@ -229,7 +265,7 @@ h3attn_status h3attn_forward_fp8(h3attn_plan_t plan, const void* q8, const void*
  * Same computation and kernel as h3attn_forward, without a plan: cu_seqlens
  * is a HOST int32 array [n_docs+1] (cu_seqlens[0] = 0, strictly increasing);
  * the work list is built on the host and, with the kernel's error word, kept
- * in one static device array of 1 MiB + 16 B that every GPU loading the
+ * in one static device array of 1 MiB + 4 KiB + 16 B that every GPU loading the
  * library holds until the process exits.  At most 32768 work units (a unit is
  * up to 512 query rows of one head in one document, so sum over documents of
  * ceil(len/512) * num_heads <= 32768); larger layouts get EINVAL with a

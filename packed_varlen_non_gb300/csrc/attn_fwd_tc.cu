@@ -410,7 +410,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t warp = dev::warp_id_uniform();
   const uint32_t lane = threadIdx.x & 31;
   const uint32_t rank = dev::cluster_ctarank();   // 0: issues the pair's MMAs
-  const int pair = (int)(blockIdx.x >> 1), n_pairs = (int)(gridDim.x >> 1);
+  const int pair = (int)(blockIdx.x >> 1);
+  // this pair's segments, in order
+  const int u_begin = __ldg(a.unit_off + pair), u_end = __ldg(a.unit_off + pair + 1);
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -473,9 +475,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       };
       int k = 0;
-      for (int u = pair; ok && u < a.n_units; u += n_pairs, ++k) {
+      for (int u = u_begin; ok && u < u_end; ++u, ++k) {
         const UnitGeom g = unit_geom(a.units, u);
-        const bool has_next = u + n_pairs < a.n_units;
+        const bool has_next = u + 1 < u_end;
         // Key/value groups: group 0 is the first unit's first K tile (ring slot
         // 0); group n >= 1 is V(j) with the next K tile -- K(j+1), or the next
         // unit's first K tile -- in slots (2n-1) % kSlots and 2n % kSlots, one
@@ -495,7 +497,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           int k_head = g.head;
           int32_t k_row = g.kv0 + (j + 1) * kTileRows;
           if (!has_k && has_next) {
-            const UnitGeom n = unit_geom(a.units, u + n_pairs);
+            const UnitGeom n = unit_geom(a.units, u + 1);
             has_k = true;
             k_head = n.head;
             k_row = n.kv0 + n.lo * kTileRows;
@@ -511,7 +513,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                               k_head, k_row, rank, pol_kv);
           ++grp;
           // the next unit's Q tiles, behind this unit's first group
-          if (j == g.lo && has_next) load_q(unit_geom(a.units, u + n_pairs), k + 1);
+          if (j == g.lo && has_next) load_q(unit_geom(a.units, u + 1), k + 1);
         }
       }
       if (!ok) {
@@ -534,67 +536,128 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       bool ok = true;
       bool issued = false;
       int k = 0;
-      for (int u = pair; ok && u < a.n_units; u += n_pairs, ++k) {
-        const UnitGeom g = unit_geom(a.units, u);
-        const uint32_t qb = 2 * (k & 1);
-        // Q tiles of this unit, prepared in both CTAs (and, for the first
-        // unit, the first K group landed in both)
+      if constexpr (kFp8) {
+        for (int u = u_begin; ok && u < u_end; ++u, ++k) {
+          const UnitGeom g = unit_geom(a.units, u);
+          const uint32_t qb = 2 * (k & 1);
+          // Q tiles of this unit, prepared in both CTAs (and, for the first
+          // unit, the first K group landed in both)
 #pragma unroll
-        for (int s = 0; s < 2; ++s) {
-          if (!ok || s >= g.n_st) break;
-          ok = dev::mbar_wait(bars.q_ready(qb + s), q_use[qb + s] & 1, abort_flag, a.err, kTimeoutNs);
-          ++q_use[qb + s];
-        }
-        // this unit's first K tile: group 0, or the K half of the previous
-        // unit's last group (covered by that unit's last P-ready barrier)
-        const uint32_t k0 = k == 0 ? 0u : (kslot >= 2 ? kslot - 2 : kslot + kSlots - 2);
-        if (!ok) break;
-        dev::tc_fence_after();
-#pragma unroll
-        for (int s = 0; s < 2; ++s) {
-          if (s >= g.n_st) break;
-          if constexpr (kFp8)
-            issue_qk_f8(tmem + s * 128, sbase + C::SmemQ + (qb + s) * C::QTileBytes,
-                        sbase + C::SmemKV + k0 * C::SlotBytes);
-          else
-            issue_qk(tmem + s * 128, sbase + C::SmemQ + (qb + s) * C::QTileBytes,
-                     sbase + C::SmemKV + k0 * C::SlotBytes);
-          dev::mma_commit_pair_mc(bars.s_ready(s), kPairMask);
-          if (g.hi - g.lo == 1) dev::mma_commit_pair_mc(bars.q_empty(qb + s), kPairMask);
-        }
-        issued = true;
-        for (int j = g.lo; j < g.hi; ++j) {
-          // group grp = V(j) + the next K tile; its arrival in both CTAs is
-          // implied by P-ready of query tile 0
-          const bool more = j + 1 < g.hi;
+          for (int s = 0; s < 2; ++s) {
+            if (!ok || s >= g.n_st) break;
+            ok = dev::mbar_wait(bars.q_ready(qb + s), q_use[qb + s] & 1, abort_flag, a.err, kTimeoutNs);
+            ++q_use[qb + s];
+          }
+          // this unit's first K tile: group 0, or the K half of the previous
+          // unit's last group (covered by that unit's last P-ready barrier)
+          const uint32_t k0 = k == 0 ? 0u : (kslot >= 2 ? kslot - 2 : kslot + kSlots - 2);
+          if (!ok) break;
+          dev::tc_fence_after();
 #pragma unroll
           for (int s = 0; s < 2; ++s) {
             if (s >= g.n_st) break;
-            uint32_t& p_it = s == 0 ? p_it0 : p_it1;
-            ok = dev::mbar_wait(bars.p_ready(s), p_it & 1, abort_flag, a.err, kTimeoutNs);
-            if (!ok) break;
-            ++p_it;
-            dev::tc_fence_after();
-            if constexpr (kFp8)
+            issue_qk_f8(tmem + s * 128, sbase + C::SmemQ + (qb + s) * C::QTileBytes,
+                        sbase + C::SmemKV + k0 * C::SlotBytes);
+            dev::mma_commit_pair_mc(bars.s_ready(s), kPairMask);
+            if (g.hi - g.lo == 1) dev::mma_commit_pair_mc(bars.q_empty(qb + s), kPairMask);
+          }
+          issued = true;
+          for (int j = g.lo; j < g.hi; ++j) {
+            // group grp = V(j) + the next K tile; its arrival in both CTAs is
+            // implied by P-ready of query tile 0
+            const bool more = j + 1 < g.hi;
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+              if (s >= g.n_st) break;
+              uint32_t& p_it = s == 0 ? p_it0 : p_it1;
+              ok = dev::mbar_wait(bars.p_ready(s), p_it & 1, abort_flag, a.err, kTimeoutNs);
+              if (!ok) break;
+              ++p_it;
+              dev::tc_fence_after();
               issue_pv_f8(tmem + 256 + s * 128, tmem + s * 128, sbase + C::SmemKV + vslot * C::SlotBytes, j > g.lo);
-            else
-              issue_pv(tmem + 256 + s * 128, tmem + s * 128, sbase + C::SmemKV + vslot * C::SlotBytes, j > g.lo);
-            if (more) {
-              if constexpr (kFp8)
+              if (more) {
                 issue_qk_f8(tmem + s * 128, sbase + C::SmemQ + (qb + s) * C::QTileBytes,
                             sbase + C::SmemKV + kslot * C::SlotBytes);
-              else
+                dev::mma_commit_pair_mc(bars.s_ready(s), kPairMask);
+                if (j + 2 == g.hi) dev::mma_commit_pair_mc(bars.q_empty(qb + s), kPairMask);
+              } else {
+                dev::mma_commit_pair_mc(bars.o_ready(s), kPairMask);
+              }
+            }
+            if (!ok) break;
+            vslot = vslot + 2 >= (uint32_t)kSlots ? vslot + 2 - kSlots : vslot + 2;
+            kslot = kslot + 2 >= (uint32_t)kSlots ? kslot + 2 - kSlots : kslot + 2;
+          }
+        }
+      } else {
+        // bf16: a unit's first QKs are issued during the last key tile of the
+        // unit before, so the tensor pipe has them queued while the softmax
+        // warps write that unit's output.
+        // The first QK of query tile s of unit gg: Q slot qbase + s (once the
+        // tile is prepared in both CTAs), K in ring slot ks.
+        auto first_qk = [&](const UnitGeom& gg, uint32_t qbase, uint32_t ks, int s) {
+          ok = dev::mbar_wait(bars.q_ready(qbase + s), q_use[qbase + s] & 1, abort_flag, a.err, kTimeoutNs);
+          ++q_use[qbase + s];
+          if (!ok) return;
+          dev::tc_fence_after();
+          issue_qk(tmem + s * 128, sbase + C::SmemQ + (qbase + s) * C::QTileBytes, sbase + C::SmemKV + ks * C::SlotBytes);
+          dev::mma_commit_pair_mc(bars.s_ready(s), kPairMask);
+          if (gg.hi - gg.lo == 1) dev::mma_commit_pair_mc(bars.q_empty(qbase + s), kPairMask);
+          issued = true;
+        };
+        for (int u = u_begin; ok && u < u_end; ++u, ++k) {
+          const UnitGeom g = unit_geom(a.units, u);
+          const uint32_t qb = 2 * (k & 1);
+          if (k == 0) {
+            // the pair's first unit: its first K tile is group 0 (ring slot
+            // 0), and Q-ready also covers that group's arrival in both CTAs
+            for (int s = 0; ok && s < g.n_st; ++s) first_qk(g, qb, 0, s);
+            if (!ok) break;
+          }
+          // The next unit's first K tile is the K half of this unit's last
+          // group (ring slot kslot in the last key tile).  Its QK of query
+          // tile s goes right after this unit's PV of tile s when the next
+          // unit has at least as many query tiles (then the MMAs that the ring
+          // release of its first key tile waits for include every PV of this
+          // unit); otherwise after both PVs.
+          const bool has_next = u + 1 < u_end;
+          const UnitGeom gn = unit_geom(a.units, has_next ? u + 1 : u);
+          const uint32_t qn = 2 * ((k + 1) & 1);
+          const bool early = has_next && gn.n_st >= g.n_st;
+          for (int j = g.lo; j < g.hi; ++j) {
+            // group grp = V(j) + the next K tile; its arrival in both CTAs is
+            // implied by P-ready of query tile 0
+            const bool more = j + 1 < g.hi;
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+              if (s >= g.n_st) break;
+              uint32_t& p_it = s == 0 ? p_it0 : p_it1;
+              ok = dev::mbar_wait(bars.p_ready(s), p_it & 1, abort_flag, a.err, kTimeoutNs);
+              if (!ok) break;
+              ++p_it;
+              dev::tc_fence_after();
+              issue_pv(tmem + 256 + s * 128, tmem + s * 128, sbase + C::SmemKV + vslot * C::SlotBytes, j > g.lo);
+              if (more) {
                 issue_qk(tmem + s * 128, sbase + C::SmemQ + (qb + s) * C::QTileBytes,
                          sbase + C::SmemKV + kslot * C::SlotBytes);
-              dev::mma_commit_pair_mc(bars.s_ready(s), kPairMask);
-              if (j + 2 == g.hi) dev::mma_commit_pair_mc(bars.q_empty(qb + s), kPairMask);
-            } else {
-              dev::mma_commit_pair_mc(bars.o_ready(s), kPairMask);
+                dev::mma_commit_pair_mc(bars.s_ready(s), kPairMask);
+                if (j + 2 == g.hi) dev::mma_commit_pair_mc(bars.q_empty(qb + s), kPairMask);
+              } else {
+                dev::mma_commit_pair_mc(bars.o_ready(s), kPairMask);
+                if (early) {
+                  first_qk(gn, qn, kslot, s);
+                  if (!ok) break;
+                }
+              }
             }
+            if (!ok) break;
+            if (!more && has_next) {
+              for (int s = early ? g.n_st : 0; ok && s < gn.n_st; ++s) first_qk(gn, qn, kslot, s);
+              if (!ok) break;
+            }
+            vslot = vslot + 2 >= (uint32_t)kSlots ? vslot + 2 - kSlots : vslot + 2;
+            kslot = kslot + 2 >= (uint32_t)kSlots ? kslot + 2 - kSlots : kslot + 2;
           }
-          if (!ok) break;
-          vslot = vslot + 2 >= (uint32_t)kSlots ? vslot + 2 - kSlots : vslot + 2;
-          kslot = kslot + 2 >= (uint32_t)kSlots ? kslot + 2 - kSlots : kslot + 2;
         }
       }
       if (!ok && issued) {
@@ -613,7 +676,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     const bool fuse_q = a.gain_q != nullptr;
     int k = 0;
-    for (int u = pair; ok && u < a.n_units; u += n_pairs, ++k) {
+    for (int u = u_begin; ok && u < u_end; ++u, ++k) {
       const UnitGeom g = unit_geom(a.units, u);
 #pragma unroll 1
       for (int s = 0; s < 2 && s < g.n_st; ++s) {
@@ -653,7 +716,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     const float sl2 = a.scale_log2;
     __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.o);
-    for (int u = pair; ok && u < a.n_units; u += n_pairs) {
+    for (int u = u_begin; ok && u < u_end; ++u) {
       const UnitGeom g = unit_geom(a.units, u);
       const uint32_t t_unit = t0;
       t0 += g.hi - g.lo;
@@ -936,9 +999,13 @@ cudaError_t launch_pairs(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
     if (why) *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
     return e;
   }
-  const int slots = forward_slots(device, num_sms);
-  const int pairs = a.n_units < slots ? a.n_units : slots;
-  attn_fwd_tc_kernel<kFp8><<<2 * pairs, kThreads, Cfg<kFp8>::SmemAlloc, stream>>>(mq, mk, mv, a);
+  (void)device;
+  (void)num_sms;
+  if (a.n_pairs < 1 || a.unit_off == nullptr) {
+    if (why) *why = "the work list has no CTA pairs";
+    return cudaErrorInvalidValue;
+  }
+  attn_fwd_tc_kernel<kFp8><<<2 * a.n_pairs, kThreads, Cfg<kFp8>::SmemAlloc, stream>>>(mq, mk, mv, a);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.n_merges == 0) return e;
   const int64_t warps = (int64_t)a.n_merges * kUnitRows;

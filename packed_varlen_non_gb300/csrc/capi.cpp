@@ -96,6 +96,11 @@ void free_plan_device(Plan* p) {
   p->d_err = nullptr;
 }
 
+// Device copy of the plan's unit_off (stored after the segment list).
+const int32_t* unit_offsets(const Plan* p) {
+  return reinterpret_cast<const int32_t*>(p->d_units + p->units_host.size());
+}
+
 h3attn_status check_plan(h3attn_plan_t plan) {
   if (plan == nullptr) return fail(H3ATTN_EINVAL, "plan is NULL");
   return H3ATTN_OK;
@@ -165,9 +170,11 @@ h3attn_status h3attn_plan_create(const h3attn_doc* docs, int32_t n_docs,
 
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
   const size_t n_cu = p->cu_host.size(), n_rope = (size_t)p->S * kRopeHalf;
+  const size_t units_bytes = p->units_host.size() * sizeof(WorkUnit),
+               off_bytes = p->unit_off_host.size() * sizeof(int32_t);
   if ((e = cudaMalloc(&p->d_cu, n_cu * sizeof(int32_t))) != cudaSuccess ||
       (e = cudaMalloc(&p->d_rope, n_rope * sizeof(float2))) != cudaSuccess ||
-      (e = cudaMalloc(&p->d_units, p->units_host.size() * sizeof(WorkUnit))) != cudaSuccess ||
+      (e = cudaMalloc(&p->d_units, units_bytes + off_bytes)) != cudaSuccess ||
       (e = cudaMalloc(&p->d_err, 16)) != cudaSuccess ||
       (e = cudaMalloc(&p->d_ktiles, p->ktiles_host.size() * sizeof(int4))) != cudaSuccess ||
       (p->n_parts > 0 &&
@@ -183,7 +190,9 @@ h3attn_status h3attn_plan_create(const h3attn_doc* docs, int32_t n_docs,
                            cudaMemcpyHostToDevice, st)) != cudaSuccess ||
       (e = cudaMemcpyAsync(p->d_rope, p->rope_host.data(), n_rope * sizeof(float2),
                            cudaMemcpyHostToDevice, st)) != cudaSuccess ||
-      (e = cudaMemcpyAsync(p->d_units, p->units_host.data(), p->units_host.size() * sizeof(WorkUnit),
+      (e = cudaMemcpyAsync(p->d_units, p->units_host.data(), units_bytes, cudaMemcpyHostToDevice, st)) !=
+          cudaSuccess ||
+      (e = cudaMemcpyAsync(p->d_units + p->units_host.size(), p->unit_off_host.data(), off_bytes,
                            cudaMemcpyHostToDevice, st)) != cudaSuccess ||
       (p->n_parts > 0 &&
        (e = cudaMemcpyAsync(p->d_merges, p->merges_host.data(), p->merges_host.size() * sizeof(MergeUnit),
@@ -330,7 +339,8 @@ static h3attn_status forward_impl(h3attn_plan_t plan, const void* q, const void*
   cudaError_t e = g.enter(plan->device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
   ForwardArgs a{q, k, v, o, lse_out, qkv_row_stride, o_row_stride, S, H,
-                softmax_scale * 1.4426950408889634f, plan->d_units, plan->n_units, plan->d_err,
+                softmax_scale * 1.4426950408889634f, plan->d_units, plan->n_units, unit_offsets(plan),
+                plan->n_pairs, plan->d_err,
                 plan->d_merges, (int32_t)plan->merges_host.size(), plan->d_part_o, plan->d_part_ml,
                 gain_q, gain_head_stride, eps, plan->d_rope};
   std::string why;
@@ -416,6 +426,40 @@ h3attn_status h3attn_plan_forward_kernels(h3attn_plan_t plan, int32_t* n_kernels
   return H3ATTN_OK;
 }
 
+h3attn_status h3attn_work_list_host(const int32_t* cu_seqlens, int32_t n_docs, int32_t num_heads,
+                                    int32_t n_pairs, int32_t* units, int64_t units_cap, int32_t* unit_off,
+                                    int64_t* n_units, int32_t* n_pairs_used) {
+  clear_error();
+  if (!cu_seqlens || !n_units || !n_pairs_used) return fail(H3ATTN_EINVAL, "NULL cu_seqlens or output count");
+  if (n_docs < 1) return fail(H3ATTN_EINVAL, "n_docs must be >= 1 (got %d)", n_docs);
+  if (num_heads < 1) return fail(H3ATTN_EINVAL, "num_heads must be >= 1 (got %d)", num_heads);
+  if (n_pairs < 1 || n_pairs > 1024) return fail(H3ATTN_EINVAL, "n_pairs must be in [1, 1024] (got %d)", n_pairs);
+  if (cu_seqlens[0] != 0) return fail(H3ATTN_EINVAL, "cu_seqlens[0] must be 0");
+  for (int32_t d = 0; d < n_docs; ++d)
+    if (cu_seqlens[d + 1] <= cu_seqlens[d])
+      return fail(H3ATTN_EINVAL, "document %d is empty or cu_seqlens is not increasing", d);
+  try {
+    std::vector<WorkUnit> all, segs;
+    std::vector<int32_t> v_off, off;
+    std::vector<MergeUnit> merges;
+    int64_t v_pad = 0;
+    int32_t pairs = 0, parts = 0;
+    const std::string why = build_units(cu_seqlens, n_docs, num_heads, all, v_off, &v_pad);
+    if (!why.empty()) return fail(H3ATTN_EINVAL, "%s", why.c_str());
+    build_segments(all, n_pairs, segs, off, &pairs, merges, &parts);
+    *n_units = (int64_t)segs.size();
+    *n_pairs_used = pairs;
+    if (units == nullptr) return H3ATTN_OK;
+    if (units_cap < (int64_t)segs.size())
+      return fail(H3ATTN_EINVAL, "units_cap %lld < %lld segments", (long long)units_cap, (long long)segs.size());
+    std::memcpy(units, segs.data(), segs.size() * sizeof(WorkUnit));
+    if (unit_off) std::memcpy(unit_off, off.data(), off.size() * sizeof(int32_t));
+  } catch (const std::bad_alloc&) {
+    return fail(H3ATTN_ENOMEM, "host allocation failed while building the work list");
+  }
+  return H3ATTN_OK;
+}
+
 h3attn_status h3attn_plan_fp8_v_keys(h3attn_plan_t plan, int64_t* v_keys) {
   clear_error();
   if (h3attn_status s = check_plan(plan)) return s;
@@ -457,7 +501,8 @@ h3attn_status h3attn_forward_fp8(h3attn_plan_t plan, const void* q8, const void*
   cudaError_t e = g.enter(plan->device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
   ForwardArgs a{q8, k8, v8t, o, lse_out, width, o_row_stride, S, H,
-                softmax_scale * 1.4426950408889634f, plan->d_units, plan->n_units, plan->d_err,
+                softmax_scale * 1.4426950408889634f, plan->d_units, plan->n_units, unit_offsets(plan),
+                plan->n_pairs, plan->d_err,
                 plan->d_merges, (int32_t)plan->merges_host.size(), plan->d_part_o, plan->d_part_ml,
                 nullptr, 0, 0.f, nullptr, sq, sk, sv, plan->v_pad};
   std::string why;

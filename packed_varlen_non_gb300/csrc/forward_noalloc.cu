@@ -12,8 +12,9 @@
 // device array instead.
 //
 // The array is a static __device__ object: every GPU that loads the library
-// holds it (16 B + 32768 x 32 B = 1 MiB + 16 B) until the process exits, all calls share
-// it, and it keeps the last call's contents.  In host code its name is only a
+// holds it (16 B + 4 KiB of per-pair offsets + 32768 x 32 B = 1 MiB + 4 KiB +
+// 16 B) until the process exits, all calls share it, and it keeps the last
+// call's contents.  In host code its name is only a
 // host-side stand-in, so the device address is taken once per device with
 // cudaGetSymbolAddress (on the first call on that device, with the device
 // current) and passed to the kernel.
@@ -28,11 +29,14 @@ namespace h3 {
 namespace {
 
 constexpr int32_t kNoAllocMaxUnits = 32768;  // work units of up to kUnitRows query rows x one head
+constexpr int32_t kNoAllocMaxPairs = 1024;   // CTA pairs the offsets can describe
+constexpr int32_t kOffsetVecs = (kNoAllocMaxPairs + 1 + 3) / 4;  // int4 holding the offsets
 constexpr int kMaxDevices = 64;
 
-// [0]: device error word (cleared before every launch); [1 ..]: work list
-// (one 32-byte record, two int4, per unit).
-static __device__ __align__(256) int4 g_noalloc_scratch[1 + 2 * kNoAllocMaxUnits];
+// [0]: device error word (cleared before every launch); [1, 1 + kOffsetVecs):
+// per-pair offsets into the work list (int32, pairs + 1 of them); then the
+// work list (one 32-byte record, two int4, per unit), grouped by pair.
+static __device__ __align__(256) int4 g_noalloc_scratch[1 + kOffsetVecs + 2 * kNoAllocMaxUnits];
 
 std::mutex g_setup_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
@@ -56,6 +60,16 @@ cudaError_t scratch_on_device(int dev, int4** out) {
 std::mutex g_stage_mutex;
 WorkUnit g_stage[kNoAllocMaxUnits];
 int32_t g_order[kNoAllocMaxUnits];
+// the image of the device array after its error word: offsets, then the placed work list
+struct StageImage {
+  int32_t unit_off[kOffsetVecs * 4];
+  WorkUnit units[kNoAllocMaxUnits];
+};
+static_assert(sizeof(StageImage) == sizeof(int4) * (kOffsetVecs + 2 * kNoAllocMaxUnits), "layout");
+StageImage g_image;
+int32_t g_pair_of[kNoAllocMaxUnits];
+int64_t g_load[kNoAllocMaxPairs];
+int32_t g_heap[kNoAllocMaxPairs];
 
 }  // namespace
 
@@ -125,6 +139,7 @@ extern "C" h3attn_status h3attn_forward_noalloc(const int32_t* cu_seqlens, int32
     return fail(H3ATTN_ECUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
 
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  int32_t n_pairs = 0;
   {
     // Same work-list order as a plan: longest documents first, then head, then query tile.
     std::lock_guard<std::mutex> lock(g_stage_mutex);
@@ -134,7 +149,8 @@ extern "C" h3attn_status h3attn_forward_noalloc(const int32_t* cu_seqlens, int32
       const int32_t lx = cu_seqlens[x + 1] - cu_seqlens[x], ly = cu_seqlens[y + 1] - cu_seqlens[y];
       return lx != ly ? lx > ly : x < y;
     });
-    // whole units only (no key-range split, so no partial buffers are needed)
+    // whole units only (no key-range split, so no partial buffers are needed),
+    // placed on the pairs as a plan places them
     int32_t nu = 0;
     for (int32_t i = 0; i < n_docs; ++i) {
       const int32_t b = cu_seqlens[g_order[i]], en = cu_seqlens[g_order[i] + 1];
@@ -142,14 +158,19 @@ extern "C" h3attn_status h3attn_forward_noalloc(const int32_t* cu_seqlens, int32
       for (int32_t h = 0; h < num_heads; ++h)
         for (int32_t r = b; r < en; r += kUnitRows) g_stage[nu++] = WorkUnit{r, b, en, h, 0, n_kv, -1, 0};
     }
+    const int slots = forward_slots(dev, sms);
+    const int grid = slots < kNoAllocMaxPairs ? slots : kNoAllocMaxPairs;
+    n_pairs = place_pairs(g_stage, (size_t)nu, grid, g_image.units, g_image.unit_off, g_pair_of, g_load, g_heap);
+    const size_t bytes = sizeof(int4) * kOffsetVecs + sizeof(WorkUnit) * (size_t)nu;
     if ((e = cudaMemsetAsync(scratch, 0, sizeof(int4), st)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(scratch + 1, g_stage, sizeof(WorkUnit) * (size_t)nu, cudaMemcpyHostToDevice,
-                             st)) != cudaSuccess)
+        (e = cudaMemcpyAsync(scratch + 1, &g_image, bytes, cudaMemcpyHostToDevice, st)) != cudaSuccess)
       return fail(H3ATTN_ECUDA, "staging the work list: %s", cudaGetErrorString(e));
   }
   ForwardArgs a{q, k, v, o, lse_out, qkv_row_stride, o_row_stride, S, num_heads,
-                softmax_scale * 1.4426950408889634f, reinterpret_cast<const WorkUnit*>(scratch + 1),
-                (int32_t)n_units, reinterpret_cast<uint32_t*>(scratch), nullptr, 0, nullptr, nullptr};
+                softmax_scale * 1.4426950408889634f,
+                reinterpret_cast<const WorkUnit*>(scratch + 1 + kOffsetVecs), (int32_t)n_units,
+                reinterpret_cast<const int32_t*>(scratch + 1), n_pairs, reinterpret_cast<uint32_t*>(scratch),
+                nullptr, 0, nullptr, nullptr};
   std::string why;
   e = launch_forward(a, dev, sms, st, &why);
   if (e != cudaSuccess)

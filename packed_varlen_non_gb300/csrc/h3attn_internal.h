@@ -53,11 +53,31 @@ struct MergeUnit {
 };
 static_assert(sizeof(MergeUnit) == 32, "MergeUnit is read as two 16-byte vectors");
 
-// Build the segment list for `grid` persistent CTA pairs: whole units in
-// round-robin rounds, then the last partial round's units split along their
-// key tiles so that every pair gets one piece (plan.cpp).
+// The attention work units of a packed layout, in list order (longest
+// document first, then head, then query rows), and each document's first key
+// in the FP8 transposed V (plan.cpp).  Returns an empty string or an error.
+std::string build_units(const int32_t* cu, int32_t n_docs, int32_t num_heads, std::vector<WorkUnit>& units,
+                        std::vector<int32_t>& v_off, int64_t* v_pad);
+
+// Estimated run time of a segment (plan.cpp), the cost its placement balances.
+int64_t segment_cost(const WorkUnit& u);
+
+// Places the n segments on `grid` persistent CTA pairs in list order, each on
+// the pair with the least estimated load so far (LPT placement; the list is
+// ordered longest document first), and writes them to `out` grouped by pair:
+// pair p runs out[unit_off[p] .. unit_off[p + 1]) in order.  Scratch: pair_of
+// [n], load and heap [grid]; unit_off has grid + 1 entries.  Returns the number
+// of pairs with work (they are pairs 0 .. that number - 1).  No allocation.
+int32_t place_pairs(const WorkUnit* segs, size_t n, int grid, WorkUnit* out, int32_t* unit_off,
+                    int32_t* pair_of, int64_t* load, int32_t* heap);
+
+// Build the segment list for `grid` persistent CTA pairs: whole units for the
+// full rounds, then the last partial round's units split along their key
+// tiles into about `grid` pieces, all placed by place_pairs (plan.cpp).
+// unit_off gets n_pairs + 1 entries.
 void build_segments(const std::vector<WorkUnit>& units, int grid, std::vector<WorkUnit>& segs,
-                    std::vector<MergeUnit>& merges, int32_t* n_parts);
+                    std::vector<int32_t>& unit_off, int32_t* n_pairs, std::vector<MergeUnit>& merges,
+                    int32_t* n_parts);
 
 struct Plan {
   int device = -1;
@@ -71,7 +91,9 @@ struct Plan {
   std::vector<int32_t> cu_host;      // [n_docs + 1]
   std::vector<double> pos_host;      // [S, 3]
   std::vector<float> rope_host;      // [S, 48, 2] (cos, sin)
-  std::vector<WorkUnit> units_host;  // segment list (see build_segments)
+  std::vector<WorkUnit> units_host;  // segment list, grouped by CTA pair (see build_segments)
+  std::vector<int32_t> unit_off_host;  // [n_pairs + 1]: pair p runs units [unit_off[p], unit_off[p + 1])
+  int32_t n_pairs = 0;
   std::vector<MergeUnit> merges_host;
   int32_t n_parts = 0;
   // every document's 128-key tiles: (begin, end, first key in the FP8
@@ -81,7 +103,7 @@ struct Plan {
 
   int32_t* d_cu = nullptr;
   float2* d_rope = nullptr;          // [S, 48] (cos, sin)
-  WorkUnit* d_units = nullptr;
+  WorkUnit* d_units = nullptr;       // the segment list, then unit_off (n_pairs + 1 int32)
   int32_t n_units = 0;
   MergeUnit* d_merges = nullptr;
   float* d_part_o = nullptr;         // [n_parts, kUnitRows, 128] unnormalised O
@@ -130,6 +152,8 @@ struct ForwardArgs {
   float scale_log2;           // softmax_scale * log2(e)
   const WorkUnit* units;
   int32_t n_units;
+  const int32_t* unit_off;    // [n_pairs + 1]: pair p runs units [unit_off[p], unit_off[p + 1])
+  int32_t n_pairs;            // CTA pairs launched
   uint32_t* err;
   const MergeUnit* merges;    // may be null when n_merges == 0
   int32_t n_merges;

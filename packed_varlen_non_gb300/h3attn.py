@@ -60,6 +60,8 @@ _SIGS = {
                             c_void_p, c_void_p, c_void_p, c_void_p],
     "h3attn_plan_fp8_v_keys": [c_void_p, POINTER(c_int64)],
     "h3attn_plan_forward_kernels": [c_void_p, POINTER(c_int32)],
+    "h3attn_work_list_host": [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_int64, c_void_p,
+                              POINTER(c_int64), POINTER(c_int32)],
     "h3attn_forward_fp8": [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
                            c_int64, c_float, c_void_p, c_void_p],
     "h3attn_forward_noalloc": [c_void_p, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_int64,
@@ -244,6 +246,24 @@ def h3attn_plan_forward_kernels(plan) -> int:
     n = c_int32()
     _check(load().h3attn_plan_forward_kernels(plan, ctypes.byref(n)), "h3attn_plan_forward_kernels")
     return n.value
+
+
+def h3attn_work_list_host(cu_seqlens, num_heads: int, n_pairs: int):
+    """The forward's work list for a layout, built on the host (no GPU needed).
+    Returns (units int32 [n, 8], unit_off int32 [pairs + 1]); the fields of a
+    unit are those of the C call."""
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int32))
+    n_docs = int(cu.size) - 1
+    n, used = c_int64(), c_int32()
+    lib = load()
+    _check(lib.h3attn_work_list_host(cu.ctypes.data, n_docs, int(num_heads), int(n_pairs), None, 0, None,
+                                     ctypes.byref(n), ctypes.byref(used)), "h3attn_work_list_host")
+    units = np.zeros((n.value, 8), dtype=np.int32)
+    off = np.zeros(used.value + 1, dtype=np.int32)
+    _check(lib.h3attn_work_list_host(cu.ctypes.data, n_docs, int(num_heads), int(n_pairs), units.ctypes.data,
+                                     n.value, off.ctypes.data, ctypes.byref(n), ctypes.byref(used)),
+           "h3attn_work_list_host")
+    return units, off
 
 
 def h3attn_plan_fp8_v_keys(plan) -> int:

@@ -48,6 +48,9 @@ EDGE_LAYOUTS = {
     "tile_boundaries": [255, 256, 257, 383, 384, 385],
     "long_ragged": [1000, 3, 513],
     "many_tiny": [int(x) for x in np.random.default_rng(11).integers(1, 40, 60)],
+    # about six units per CTA pair, consecutive units switching between one
+    # and two active query tiles and between one and several key tiles
+    "mixed_query_tiles": [700, 600, 200, 300, 100, 128, 257, 1, 513] * 12,
 }
 
 
