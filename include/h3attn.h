@@ -197,6 +197,23 @@ h3attn_status h3attn_fp8_quantize(h3attn_plan_t plan, const void* q_hat, const v
                                   int64_t qkv_row_stride, void* q8, void* k8, void* v8t, float* sq, float* sk,
                                   float* sv, void* cuda_stream);
 
+/* The q/k prologue and the FP8 quantisation in one call, for the FP8 step:
+ * the same codes and scales as h3attn_qk_prologue (gains and eps as there)
+ * followed by h3attn_fp8_quantize on its bf16 outputs and on v, without
+ * q-hat and k-hat ever being written.  q_in, k_in, v: bf16 [S,H,128] with
+ * qkv_row_stride (a fused-qkv buffer works); q8, k8, v8t, sq, sk, sv: as
+ * h3attn_fp8_quantize writes them.  One kernel normalises, rotates, rounds
+ * to bf16 and quantises q per row and k per document key tile (one block per
+ * key tile and head, the tile's k rows held on chip until its amax is
+ * known); v takes the two passes of h3attn_fp8_quantize.  All buffers are
+ * caller-owned device memory, 16-byte aligned; no output may overlap an input
+ * or another output.  Errors: EINVAL for null/misaligned pointers, a bad
+ * stride, gain_head_stride or eps, and overlaps. */
+h3attn_status h3attn_qk_prologue_fp8(h3attn_plan_t plan, const void* q_in, const void* k_in, const void* v,
+                                     int64_t qkv_row_stride, const float* gain_q, const float* gain_k,
+                                     int64_t gain_head_stride, float eps, void* q8, void* k8, void* v8t, float* sq,
+                                     float* sk, float* sv, void* cuda_stream);
+
 /* Kernels one h3attn_forward call launches with this plan: 1, or 2 when the
  * last round of work units is split along the keys and merged. */
 h3attn_status h3attn_plan_forward_kernels(h3attn_plan_t plan, int32_t* n_kernels);

@@ -376,14 +376,14 @@ h3attn_status h3attn_forward_fused_q(h3attn_plan_t plan, const void* q_raw, cons
                       gain_head_stride, eps, cuda_stream);
 }
 
-h3attn_status h3attn_fp8_quantize(h3attn_plan_t plan, const void* q_hat, const void* k_hat, const void* v,
-                                  int64_t qkv_row_stride, void* q8, void* k8, void* v8t, float* sq, float* sk,
-                                  float* sv, void* cuda_stream) {
-  clear_error();
-  if (h3attn_status s = check_plan(plan)) return s;
-  if (!q_hat || !k_hat || !v || !q8 || !k8 || !v8t || !sq || !sk || !sv)
+// Checks shared by the FP8 quantisation calls: the three bf16 inputs (row
+// stride qkv_row_stride) and the six outputs are non-NULL and 16-byte
+// aligned, and no output shares bytes with an input or another output.
+static h3attn_status check_fp8_io(const Plan* plan, const void* const (&in)[3], int64_t qkv_row_stride, void* q8,
+                                  void* k8, void* v8t, float* sq, float* sk, float* sv) {
+  if (!in[0] || !in[1] || !in[2] || !q8 || !k8 || !v8t || !sq || !sk || !sv)
     return fail(H3ATTN_EINVAL, "NULL tensor or scale pointer");
-  if (!aligned16(q_hat) || !aligned16(k_hat) || !aligned16(v) || !aligned16(q8) || !aligned16(k8) ||
+  if (!aligned16(in[0]) || !aligned16(in[1]) || !aligned16(in[2]) || !aligned16(q8) || !aligned16(k8) ||
       !aligned16(v8t) || !aligned16(sq) || !aligned16(sk) || !aligned16(sv))
     return fail(H3ATTN_EINVAL, "tensors and scales must be 16-byte aligned");
   const int64_t width = (int64_t)plan->num_heads * kHeadDim;
@@ -392,9 +392,8 @@ h3attn_status h3attn_fp8_quantize(h3attn_plan_t plan, const void* q_hat, const v
   const int64_t S = plan->S;
   const int32_t H = plan->num_heads;
   const int64_t v_pad = plan->v_pad;
-  // outputs must not share bytes with the inputs or with each other
-  const uintptr_t in_lo[3] = {reinterpret_cast<uintptr_t>(q_hat), reinterpret_cast<uintptr_t>(k_hat),
-                              reinterpret_cast<uintptr_t>(v)};
+  const uintptr_t in_lo[3] = {reinterpret_cast<uintptr_t>(in[0]), reinterpret_cast<uintptr_t>(in[1]),
+                              reinterpret_cast<uintptr_t>(in[2])};
   const uintptr_t in_len = (uintptr_t)(((S - 1) * qkv_row_stride + width) * 2);
   const uintptr_t out_lo[6] = {reinterpret_cast<uintptr_t>(q8), reinterpret_cast<uintptr_t>(k8),
                                reinterpret_cast<uintptr_t>(v8t), reinterpret_cast<uintptr_t>(sq),
@@ -409,13 +408,47 @@ h3attn_status h3attn_fp8_quantize(h3attn_plan_t plan, const void* q_hat, const v
       if (out_lo[o] < out_lo[o2] + out_len[o2] && out_lo[o2] < out_lo[o] + out_len[o])
         return fail(H3ATTN_EINVAL, "two outputs overlap");
   }
+  return H3ATTN_OK;
+}
+
+h3attn_status h3attn_fp8_quantize(h3attn_plan_t plan, const void* q_hat, const void* k_hat, const void* v,
+                                  int64_t qkv_row_stride, void* q8, void* k8, void* v8t, float* sq, float* sk,
+                                  float* sv, void* cuda_stream) {
+  clear_error();
+  if (h3attn_status s = check_plan(plan)) return s;
+  const void* const in[3] = {q_hat, k_hat, v};
+  if (h3attn_status s = check_fp8_io(plan, in, qkv_row_stride, q8, k8, v8t, sq, sk, sv)) return s;
   DeviceGuard g;
   cudaError_t e = g.enter(plan->device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
-  Fp8QuantArgs a{q_hat, k_hat, v, qkv_row_stride, S, H, plan->d_ktiles, (int32_t)plan->ktiles_host.size(),
-                 q8, k8, v8t, v_pad, sq, sk, sv};
+  Fp8QuantArgs a{q_hat, k_hat, v, qkv_row_stride, plan->S, plan->num_heads, plan->d_ktiles,
+                 (int32_t)plan->ktiles_host.size(), q8, k8, v8t, plan->v_pad, sq, sk, sv};
   e = launch_fp8_quantize(a, plan->num_sms, static_cast<cudaStream_t>(cuda_stream));
   return e == cudaSuccess ? H3ATTN_OK : cuda_fail(e, "fp8 quantise launch");
+}
+
+h3attn_status h3attn_qk_prologue_fp8(h3attn_plan_t plan, const void* q_in, const void* k_in, const void* v,
+                                     int64_t qkv_row_stride, const float* gain_q, const float* gain_k,
+                                     int64_t gain_head_stride, float eps, void* q8, void* k8, void* v8t, float* sq,
+                                     float* sk, float* sv, void* cuda_stream) {
+  clear_error();
+  if (h3attn_status s = check_plan(plan)) return s;
+  if (!gain_q || !gain_k) return fail(H3ATTN_EINVAL, "NULL gain pointer");
+  if (!aligned16(gain_q) || !aligned16(gain_k)) return fail(H3ATTN_EINVAL, "gains must be 16-byte aligned");
+  if (gain_head_stride != 0 && (gain_head_stride < kHeadDim || (gain_head_stride % 4)))
+    return fail(H3ATTN_EINVAL, "gain_head_stride must be 0 or >= 128 and a multiple of 4");
+  if (!std::isfinite(eps) || eps < 0.f) return fail(H3ATTN_EINVAL, "eps must be finite and >= 0");
+  const void* const in[3] = {q_in, k_in, v};
+  if (h3attn_status s = check_fp8_io(plan, in, qkv_row_stride, q8, k8, v8t, sq, sk, sv)) return s;
+  DeviceGuard g;
+  cudaError_t e = g.enter(plan->device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+  const PrologueArgs p{q_in, k_in, nullptr, nullptr, qkv_row_stride, 0, gain_q, gain_k, gain_head_stride,
+                       plan->d_rope, plan->S, plan->num_heads, eps};
+  const Fp8QuantArgs a{nullptr, nullptr, v, qkv_row_stride, plan->S, plan->num_heads, plan->d_ktiles,
+                       (int32_t)plan->ktiles_host.size(), q8, k8, v8t, plan->v_pad, sq, sk, sv};
+  e = launch_prologue_fp8(p, a, static_cast<cudaStream_t>(cuda_stream));
+  return e == cudaSuccess ? H3ATTN_OK : cuda_fail(e, "fp8 prologue launch");
 }
 
 h3attn_status h3attn_plan_forward_kernels(h3attn_plan_t plan, int32_t* n_kernels) {

@@ -16,6 +16,7 @@
 #include <cuda_bf16.h>
 
 #include "device_common.cuh"
+#include "qk_norm.cuh"
 
 namespace h3 {
 
@@ -134,6 +135,130 @@ __global__ void __launch_bounds__(256) quant_ktiles_kernel(Fp8QuantArgs a) {
   }
 }
 
+// The q/k prologue and the q/k quantisation in one pass (h3attn_qk_prologue_fp8):
+// the prologue's RMSNorm + rot96 arithmetic (qk_norm.cuh), its bf16 rounding,
+// then the codes and scales of quant_rows_kernel and quant_ktiles_kernel from
+// those bf16 values -- the same bits as the three kernels in turn, without
+// q-hat and k-hat going through HBM.  The block also folds its tile's v rows
+// into the per-channel maxima (vmax_kernel's job).  One block per (key tile,
+// head), 16 lanes per token row: thread i takes dims [8 (i%16), +8) of
+// tokens b + i/16 + 16u (u < 8), four rows at a time whose q and k loads it
+// issues together before working on them (80 registers: three blocks per SM).
+// A q row is quantised as soon as it is normalised; the k rows wait in shared
+// memory (bf16) until the tile's amax is known.
+__global__ void __launch_bounds__(256, 3) prologue_quant_kernel(PrologueArgs p, Fp8QuantArgs a) {
+  __shared__ uint4 k_tile[128][16];     // the tile's k-hat rows, bf16 (32 KB)
+  __shared__ float warp_max[8];
+  __shared__ float v_max[8][kHeadDim];  // per warp, per channel
+  const int4 te = a.tiles[blockIdx.x];
+  const int h = blockIdx.y;
+  const int lane16 = threadIdx.x & 15, tl0 = threadIdx.x >> 4, warp = threadIdx.x >> 5;
+  const unsigned mask = 0xffffu << (threadIdx.x & 16);
+  const __nv_bfloat16* qi = static_cast<const __nv_bfloat16*>(p.q_in) + h * kHeadDim + lane16 * 8;
+  const __nv_bfloat16* ki = static_cast<const __nv_bfloat16*>(p.k_in) + h * kHeadDim + lane16 * 8;
+  const __nv_bfloat16* vi = static_cast<const __nv_bfloat16*>(a.v) + h * kHeadDim + lane16 * 8;
+  const float* gq = p.gain_q + h * p.gain_head_stride;
+  const float* gk = p.gain_k + h * p.gain_head_stride;
+  uint8_t* q8 = static_cast<uint8_t*>(a.q8) + h * kHeadDim + lane16 * 8;
+  // rows of this lane group: tokens te.x + tl0 + 16 u for u < n_rows
+  const int rem = te.y - te.x - tl0;
+  const int n_rows = rem > 0 ? (rem + 15) / 16 : 0;
+  // Straight-line over each batch's rows (the next row's table loads can then
+  // be issued early): a row past the tile end is all zeros, stays zero through
+  // the norm and rotation (its table row is the tile's first), and is not
+  // stored.
+  float kmax = 0.f;
+#pragma unroll 1
+  for (int half = 0; half < 2; ++half) {
+    uint4 kraw[4], qraw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int u = 4 * half + i;
+      const int64_t t = te.x + tl0 + 16 * u;
+      if (u < n_rows) {
+        kraw[i] = __ldcs(reinterpret_cast<const uint4*>(ki + t * p.in_stride));
+        qraw[i] = __ldcs(reinterpret_cast<const uint4*>(qi + t * p.in_stride));
+      } else {
+        kraw[i] = qraw[i] = make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int u = 4 * half + i;
+      const bool valid = u < n_rows;
+      const int64_t t = te.x + tl0 + 16 * u;
+      float c[8], s[8];
+      qkn::load_cs16(p.rope, valid ? t : (int64_t)te.x, lane16, c, s);
+      float x[8];
+      qkn::unpack8(kraw[i], x);
+      qkn::norm_rope16(x, gk, c, s, lane16, mask, p.eps);
+      const uint4 kb = qkn::pack8(x);
+      k_tile[tl0 + 16 * u][lane16] = kb;
+      qkn::unpack8(kb, x);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) kmax = fmaxf(kmax, fabsf(x[e]));
+      qkn::unpack8(qraw[i], x);
+      qkn::norm_rope16(x, gq, c, s, lane16, mask, p.eps);
+      qkn::unpack8(qkn::pack8(x), x);
+      float m = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) m = fmaxf(m, fabsf(x[e]));
+#pragma unroll
+      for (int off = 8; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(mask, m, off, 16));
+      if (valid) {
+        *reinterpret_cast<uint2*>(q8 + t * a.H * kHeadDim) = codes8(x, fp8_recip(m));
+        if (lane16 == 0) a.sq[(int64_t)h * a.S + t] = fp8_scale(m);
+      }
+    }
+  }
+  // v: this thread's channel maxima over its rows
+  uint4 vraw[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    vraw[u] = u < n_rows ? __ldcs(reinterpret_cast<const uint4*>(vi + (int64_t)(te.x + tl0 + 16 * u) * a.stride))
+                         : make_uint4(0, 0, 0, 0);
+  float vm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    float x[8];
+    qkn::unpack8(vraw[u], x);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) vm[e] = fmaxf(vm[e], fabsf(x[e]));
+  }
+  // block maxima: k over the tile, v per channel (rows past the tile end count as 0)
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) kmax = fmaxf(kmax, __shfl_xor_sync(0xffffffffu, kmax, off));
+#pragma unroll
+  for (int e = 0; e < 8; ++e) vm[e] = fmaxf(vm[e], __shfl_xor_sync(0xffffffffu, vm[e], 16));
+  if ((threadIdx.x & 31) == 0) warp_max[warp] = kmax;
+  if ((threadIdx.x & 16) == 0) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v_max[warp][lane16 * 8 + e] = vm[e];
+  }
+  __syncthreads();
+  if (threadIdx.x < kHeadDim) {
+    float m = v_max[0][threadIdx.x];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) m = fmaxf(m, v_max[w][threadIdx.x]);
+    // non-negative floats order like their bit patterns
+    atomicMax(reinterpret_cast<uint32_t*>(a.sv) + h * kHeadDim + threadIdx.x, __float_as_uint(m));
+  }
+  float m = warp_max[0];
+#pragma unroll
+  for (int w = 1; w < 8; ++w) m = fmaxf(m, warp_max[w]);
+  const float r = fp8_recip(m), sc = fp8_scale(m);
+  uint8_t* k8 = static_cast<uint8_t*>(a.k8) + h * kHeadDim + lane16 * 8;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    if (u >= n_rows) break;
+    const int64_t t = te.x + tl0 + 16 * u;
+    float x[8];
+    qkn::unpack8(k_tile[tl0 + 16 * u][lane16], x);
+    *reinterpret_cast<uint2*>(k8 + t * a.H * kHeadDim) = codes8(x, r);
+    if (lane16 == 0) a.sk[(int64_t)h * a.S + t] = sc;
+  }
+}
+
 // v, pass 1: per-(head, channel) amax over all tokens into the scale buffer's
 // bits (non-negative floats order like their bit patterns).  Block (x, y):
 // 128 groups of 8 channels from group 128 x, tokens [64 y, 64 y + 64);
@@ -207,6 +332,13 @@ __global__ void vscale_kernel(Fp8QuantArgs a) {
   if (i < a.H * kHeadDim) a.sv[i] = fp8_scale(__uint_as_float(reinterpret_cast<const uint32_t*>(a.sv)[i]));
 }
 
+// v: codes (transposed) and scales, once sv holds the channel maxima' bits
+cudaError_t launch_v_codes(const Fp8QuantArgs& a, cudaStream_t stream) {
+  vquant_kernel<<<dim3(a.n_tiles, a.H), 256, 0, stream>>>(a);
+  vscale_kernel<<<(a.H * kHeadDim + 255) / 256, 256, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_fp8_quantize(const Fp8QuantArgs& a, int num_sms, cudaStream_t stream) {
@@ -220,9 +352,15 @@ cudaError_t launch_fp8_quantize(const Fp8QuantArgs& a, int num_sms, cudaStream_t
   if (e != cudaSuccess) return e;
   vmax_kernel<<<dim3((unsigned)((a.H * 16 + 127) / 128), (unsigned)((a.S + kVmaxTokens - 1) / kVmaxTokens)), 128, 0,
                  stream>>>(a);
-  vquant_kernel<<<dim3(a.n_tiles, a.H), 256, 0, stream>>>(a);
-  vscale_kernel<<<(a.H * kHeadDim + 255) / 256, 256, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_v_codes(a, stream);
+}
+
+cudaError_t launch_prologue_fp8(const PrologueArgs& p, const Fp8QuantArgs& a, cudaStream_t stream) {
+  if (a.S == 0) return cudaSuccess;
+  cudaError_t e = cudaMemsetAsync(a.sv, 0, (size_t)a.H * kHeadDim * sizeof(float), stream);
+  if (e != cudaSuccess) return e;
+  prologue_quant_kernel<<<dim3(a.n_tiles, a.H), 256, 0, stream>>>(p, a);
+  return launch_v_codes(a, stream);
 }
 
 }  // namespace h3

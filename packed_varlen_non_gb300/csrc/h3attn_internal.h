@@ -199,6 +199,9 @@ struct Fp8QuantArgs {
   float* sv;                   // [H, 128]
 };
 cudaError_t launch_fp8_quantize(const Fp8QuantArgs& a, int num_sms, cudaStream_t stream);
+// The prologue fused with the q/k quantisation (p: inputs, gains, table; a:
+// v and the FP8 outputs), then the v quantisation (fp8_quant.cu).
+cudaError_t launch_prologue_fp8(const PrologueArgs& p, const Fp8QuantArgs& a, cudaStream_t stream);
 
 cudaError_t launch_selftest_bounded_wait(uint64_t timeout_ns, uint32_t* d_flag,
                                          cudaStream_t stream);

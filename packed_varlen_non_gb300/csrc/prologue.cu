@@ -27,37 +27,6 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kRowsPerBlock = kThreads / 16;
 
-// Normalise x (this lane's 8 dims of one row), apply gain and the rotation
-// (the arithmetic of qk_norm.cuh, spread over 16 lanes).
-__device__ __forceinline__ void norm_rope(float (&x)[8], const float* gain, const float (&c)[8],
-                                          const float (&s)[8], int lane16, unsigned mask,
-                                          float eps) {
-  float ss = qkn::chunk_ss(x);
-#pragma unroll
-  for (int off = 8; off > 0; off >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(mask, ss, off, 16));
-  const float r = qkn::inv_rms(ss, eps);
-  const float4 g0 = __ldg(reinterpret_cast<const float4*>(gain + lane16 * 8));
-  const float4 g1 = __ldg(reinterpret_cast<const float4*>(gain + lane16 * 8 + 4));
-  const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-  float y[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) y[e] = qkn::scale_gain(x[e], r, g[e]);
-  const int partner = lane16 < 6 ? lane16 + 6 : (lane16 < 12 ? lane16 - 6 : lane16);
-  float p[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) p[e] = __shfl_sync(mask, y[e], partner, 16);
-  if (lane16 < 6) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = qkn::rot_lo(y[e], p[e], c[e], s[e]);
-  } else if (lane16 < 12) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = qkn::rot_hi(y[e], p[e], c[e], s[e]);
-  } else {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = y[e];
-  }
-}
-
 __global__ void __launch_bounds__(kThreads) qk_prologue_kernel(PrologueArgs a) {
   const int lane16 = threadIdx.x & 15;
   const unsigned mask = 0xffffu << (threadIdx.x & 16);
@@ -77,33 +46,16 @@ __global__ void __launch_bounds__(kThreads) qk_prologue_kernel(PrologueArgs a) {
     const uint4 kraw = __ldcs(reinterpret_cast<const uint4*>(ki + in_off));
     const uint4 qraw = with_q ? __ldcs(reinterpret_cast<const uint4*>(qi + in_off)) : make_uint4(0, 0, 0, 0);
     float c[8], s[8];
-    if (lane16 < 12) {
-      const float4* t =
-          reinterpret_cast<const float4*>(a.rope + tok * kRopeHalf + (lane16 % 6) * 8);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4 cs = __ldg(t + i);  // (cos, sin) of two consecutive angles
-        c[2 * i] = cs.x;
-        s[2 * i] = cs.y;
-        c[2 * i + 1] = cs.z;
-        s[2 * i + 1] = cs.w;
-      }
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        c[e] = 1.f;
-        s[e] = 0.f;
-      }
-    }
+    qkn::load_cs16(a.rope, tok, lane16, c, s);
     float xk[8];
     qkn::unpack8(kraw, xk);
-    norm_rope(xk, a.gain_k + head * a.gain_head_stride, c, s, lane16, mask, a.eps);
+    qkn::norm_rope16(xk, a.gain_k + head * a.gain_head_stride, c, s, lane16, mask, a.eps);
     const int64_t out_off = tok * a.out_stride + head * kHeadDim + lane16 * 8;
     __stcs(reinterpret_cast<uint4*>(ko + out_off), qkn::pack8(xk));
     if (with_q) {
       float xq[8];
       qkn::unpack8(qraw, xq);
-      norm_rope(xq, a.gain_q + head * a.gain_head_stride, c, s, lane16, mask, a.eps);
+      qkn::norm_rope16(xq, a.gain_q + head * a.gain_head_stride, c, s, lane16, mask, a.eps);
       __stcs(reinterpret_cast<uint4*>(qo + out_off), qkn::pack8(xq));
     }
   }

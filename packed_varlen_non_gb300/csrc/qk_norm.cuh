@@ -75,5 +75,60 @@ __device__ __forceinline__ float rot_hi(float y, float partner, float c, float s
   return __fmaf_rn(y, c, __fmul_rn(partner, s));
 }
 
+// cos/sin of the 8 angles of lane lane16 of a 16-lane row group for token
+// tok (lanes j and j + 6 share angles 8 (j % 6) .. + 8; lanes 12..15, the
+// unrotated dims, get cos 1, sin 0).  rope: [S, 48] (cos, sin).
+__device__ __forceinline__ void load_cs16(const float2* rope, int64_t tok, int lane16, float (&c)[8], float (&s)[8]) {
+  if (lane16 < 12) {
+    const float4* t = reinterpret_cast<const float4*>(rope + tok * kRopeHalf + (lane16 % 6) * 8);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 cs = __ldg(t + i);  // (cos, sin) of two consecutive angles
+      c[2 * i] = cs.x;
+      s[2 * i] = cs.y;
+      c[2 * i + 1] = cs.z;
+      s[2 * i + 1] = cs.w;
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      c[e] = 1.f;
+      s[e] = 0.f;
+    }
+  }
+}
+
+// One row spread over 16 lanes (lane16 = lane within its group of 16, mask =
+// the group's lanes): normalise x (this lane's 8 dims), apply the gain and
+// the rotation.  c, s: cos/sin of this lane's 8 angles (1, 0 for lanes 12..15).
+__device__ __forceinline__ void norm_rope16(float (&x)[8], const float* gain, const float (&c)[8],
+                                          const float (&s)[8], int lane16, unsigned mask,
+                                          float eps) {
+  float ss = chunk_ss(x);
+#pragma unroll
+  for (int off = 8; off > 0; off >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(mask, ss, off, 16));
+  const float r = inv_rms(ss, eps);
+  const float4 g0 = __ldg(reinterpret_cast<const float4*>(gain + lane16 * 8));
+  const float4 g1 = __ldg(reinterpret_cast<const float4*>(gain + lane16 * 8 + 4));
+  const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+  float y[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) y[e] = scale_gain(x[e], r, g[e]);
+  const int partner = lane16 < 6 ? lane16 + 6 : (lane16 < 12 ? lane16 - 6 : lane16);
+  float p[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) p[e] = __shfl_sync(mask, y[e], partner, 16);
+  if (lane16 < 6) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = rot_lo(y[e], p[e], c[e], s[e]);
+  } else if (lane16 < 12) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = rot_hi(y[e], p[e], c[e], s[e]);
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = y[e];
+  }
+}
+
 }  // namespace qkn
 }  // namespace h3

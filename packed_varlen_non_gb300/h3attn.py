@@ -60,6 +60,8 @@ _SIGS = {
                             c_void_p, c_void_p, c_void_p, c_void_p],
     "h3attn_plan_fp8_v_keys": [c_void_p, POINTER(c_int64)],
     "h3attn_plan_forward_kernels": [c_void_p, POINTER(c_int32)],
+    "h3attn_qk_prologue_fp8": [c_void_p, c_void_p, c_void_p, c_void_p, c_int64, c_void_p, c_void_p, c_int64,
+                               c_float, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p],
     "h3attn_work_list_host": [c_void_p, c_int32, c_int32, c_int32, c_void_p, c_int64, c_void_p,
                               POINTER(c_int64), POINTER(c_int32)],
     "h3attn_forward_fp8": [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p,
@@ -240,6 +242,19 @@ def h3attn_fp8_quantize(plan, q_hat, k_hat, v, q8, k8, v8t, sq, sk, sv, qkv_row_
     _check(load().h3attn_fp8_quantize(plan, _ptr(q_hat), _ptr(k_hat), _ptr(v), _row_stride(q_hat, qkv_row_stride),
                                       _ptr(q8), _ptr(k8), _ptr(v8t), _ptr(sq), _ptr(sk), _ptr(sv), _stream(stream)),
            "h3attn_fp8_quantize")
+
+
+def h3attn_qk_prologue_fp8(plan, q_in, k_in, v, gain_q, gain_k, eps: float, q8, k8, v8t, sq, sk, sv,
+                           gain_head_stride: int = 0, qkv_row_stride=None, stream=None):
+    """The q/k prologue fused with the FP8 quantisation (see include/h3attn.h)."""
+    if qkv_row_stride is None and not isinstance(q_in, int):
+        strides = {int(x.stride(0)) for x in (q_in, k_in, v)}
+        if len(strides) != 1:
+            raise ValueError(f"q, k and v must share one row stride (got {sorted(strides)})")
+    _check(load().h3attn_qk_prologue_fp8(plan, _ptr(q_in), _ptr(k_in), _ptr(v), _row_stride(q_in, qkv_row_stride),
+                                         _ptr(gain_q), _ptr(gain_k), int(gain_head_stride), float(eps), _ptr(q8),
+                                         _ptr(k8), _ptr(v8t), _ptr(sq), _ptr(sk), _ptr(sv), _stream(stream)),
+           "h3attn_qk_prologue_fp8")
 
 
 def h3attn_plan_forward_kernels(plan) -> int:

@@ -174,3 +174,110 @@ def test_fp8_rejects_bad_arguments(lib):
         H.h3attn_forward_fp8(plan.handle, *args, o, 0.1)
         H.h3attn_get_device_error(plan.handle)
         assert H.h3attn_plan_forward_kernels(plan.handle) in (1, 2)
+
+
+def fused_vs_two_calls(docs, Hh, t, fused_qkv=False, per_head_gains=False):
+    """h3attn_qk_prologue_fp8 against h3attn_qk_prologue + h3attn_fp8_quantize:
+    every code and scale bit-identical (and the transposed V's gaps zero)."""
+    dev = torch.device("cuda")
+    S = int(t.q.shape[0])
+    W = Hh * 128
+    if fused_qkv:  # q, k, v as views of one [S, 3 W] buffer
+        buf = torch.empty(S, 3 * W, dtype=torch.bfloat16, device=dev)
+        q, k, v = buf[:, :W], buf[:, W:2 * W], buf[:, 2 * W:]
+        for dst, bits in ((q, t.q), (k, t.k), (v, t.v)):
+            dst.copy_(bf16_to_torch(bits).view(S, W))
+    else:
+        q, k, v = (bf16_to_torch(x).view(S, W) for x in (t.q, t.k, t.v))
+    if per_head_gains:
+        rng = np.random.default_rng(5)
+        gq = torch.from_numpy((1 + 0.1 * rng.standard_normal((Hh, 128))).astype(np.float32)).to(dev)
+        gk = torch.from_numpy((1 + 0.1 * rng.standard_normal((Hh, 128))).astype(np.float32)).to(dev)
+        ghs = 128
+    else:
+        gq, gk, ghs = torch.from_numpy(t.gain_q).to(dev), torch.from_numpy(t.gain_k).to(dev), 0
+    with H.Plan(docs, Hh) as plan:
+        vk = H.h3attn_plan_fp8_v_keys(plan.handle)
+        qh = torch.empty(S, W, dtype=torch.bfloat16, device=dev)
+        kh = torch.empty_like(qh)
+        H.h3attn_qk_prologue(plan.handle, q, k, qh, kh, gq, gk, 1e-6, gain_head_stride=ghs)
+        a = fp8_buffers(S, Hh, vk)
+        H.h3attn_fp8_quantize(plan.handle, qh, kh, v.contiguous(), a["q8"], a["k8"], a["v8t"], a["sq"], a["sk"],
+                              a["sv"])
+        b = fp8_buffers(S, Hh, vk)
+        H.h3attn_qk_prologue_fp8(plan.handle, q, k, v, gq, gk, 1e-6, b["q8"], b["k8"], b["v8t"], b["sq"], b["sk"],
+                                 b["sv"], gain_head_stride=ghs)
+        H.h3attn_get_device_error(plan.handle)
+        for n in a:
+            assert torch.equal(a[n], b[n]), f"{n} differs between the fused and the two-call paths"
+
+
+@pytest.mark.parametrize("case", ["ragged", "grid_video", "ref2va", "fused_qkv_per_head_gains"])
+def test_prologue_fp8_matches_prologue_then_quantize(lib, case):
+    if case == "ragged":
+        lens, Hh = [1000, 3, 513, 129, 1], 3
+        fused_vs_two_calls(docs_1d(lens), Hh, random_tensors(sum(lens), Hh, seed=41))
+    elif case in ("grid_video", "ref2va"):
+        w = synth.config(2 if case == "grid_video" else 3)
+        fused_vs_two_calls(synth.spans_to_tuples(w.docs), w.num_heads, synth.make_tensors(w))
+    else:
+        lens, Hh = [777, 300, 64], 7
+        fused_vs_two_calls(docs_1d(lens), Hh, random_tensors(sum(lens), Hh, seed=43), fused_qkv=True,
+                           per_head_gains=True)
+
+
+def test_prologue_fp8_forward_within_bound(lib):
+    # the FP8 step through the fused call, against exact attention on the
+    # dequantised values of the oracle's own quantisation of the bf16 prologue
+    from oracle import attention as oatt
+    lens, Hh = [700, 129, 1, 300], 2
+    S = sum(lens)
+    W = Hh * 128
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    scale = 1.0 / np.sqrt(128.0)
+    t = random_tensors(S, Hh, seed=47)
+    dev = torch.device("cuda")
+    q, k, v = (bf16_to_torch(x).view(S, W) for x in (t.q, t.k, t.v))
+    gq, gk = torch.from_numpy(t.gain_q).to(dev), torch.from_numpy(t.gain_k).to(dev)
+    with H.Plan(docs_1d(lens), Hh) as plan:
+        qh, kh = torch.empty_like(q), torch.empty_like(k)
+        H.h3attn_qk_prologue(plan.handle, q, k, qh, kh, gq, gk, 1e-6)
+        b = fp8_buffers(S, Hh, H.h3attn_plan_fp8_v_keys(plan.handle))
+        H.h3attn_qk_prologue_fp8(plan.handle, q, k, v, gq, gk, 1e-6, b["q8"], b["k8"], b["v8t"], b["sq"], b["sk"],
+                                 b["sv"])
+        o = torch.full((S, W), float("nan"), dtype=torch.bfloat16, device=dev)
+        H.h3attn_forward_fp8(plan.handle, b["q8"], b["k8"], b["v8t"], b["sq"], b["sk"], b["sv"], o, scale)
+        H.h3attn_get_device_error(plan.handle)
+        o = o.double().cpu().numpy().reshape(S, Hh, 128)
+        qh = qh.double().cpu().numpy().reshape(S, Hh, 128)
+        kh = kh.double().cpu().numpy().reshape(S, Hh, 128)
+    q8, sq, k8, sk, v8, sv = ofp8.quantize(qh, kh, synth.bf16_bits_to_f64(t.v), cu)
+    assert np.array_equal(b["q8"].cpu().numpy().reshape(S, Hh, 128), q8)
+    assert np.array_equal(b["k8"].cpu().numpy().reshape(S, Hh, 128), k8)
+    assert np.array_equal(b["sk"].cpu().numpy(), sk) and np.array_equal(b["sv"].cpu().numpy(), sv)
+    qd, kd, vd = ofp8.dequantize(q8, sq, k8, sk, v8, sv)
+    rows = np.arange(S)
+    o_ref, _ = oatt.attention_rows(qd, kd, vd, cu, scale, range(Hh), rows)
+    tol = ofp8.error_bound(qd, kd, vd, cu, scale, range(Hh), rows) + 2.0 ** -8 * np.abs(o_ref) + 1e-4
+    assert np.all(np.abs(o - o_ref) <= tol)
+
+
+def test_prologue_fp8_rejects_bad_arguments(lib):
+    lens, Hh = [300, 40], 2
+    S = sum(lens)
+    dev = torch.device("cuda")
+    x = torch.zeros(S, Hh * 128, dtype=torch.bfloat16, device=dev)
+    g = torch.ones(128, dtype=torch.float32, device=dev)
+    with H.Plan(docs_1d(lens), Hh) as plan:
+        b = fp8_buffers(S, Hh, H.h3attn_plan_fp8_v_keys(plan.handle))
+        outs = [b["q8"], b["k8"], b["v8t"], b["sq"], b["sk"], b["sv"]]
+        for call in (lambda: H.h3attn_qk_prologue_fp8(plan.handle, x, x, x, None, g, 1e-6, *outs),
+                     lambda: H.h3attn_qk_prologue_fp8(plan.handle, x, x, x, g, g, -1.0, *outs),
+                     lambda: H.h3attn_qk_prologue_fp8(plan.handle, x, x, x, g, g, 1e-6, *outs, gain_head_stride=64),
+                     lambda: H.h3attn_qk_prologue_fp8(plan.handle, x, x, x, g, g, 1e-6,
+                                                      x.view(torch.uint8)[:, :Hh * 128], *outs[1:])):
+            with pytest.raises(H.H3AttnError) as e:
+                call()
+            assert e.value.status == H.H3ATTN_EINVAL
+        H.h3attn_qk_prologue_fp8(plan.handle, x, x, x, g, g, 1e-6, *outs)  # a valid call still works
+        H.h3attn_get_device_error(plan.handle)
