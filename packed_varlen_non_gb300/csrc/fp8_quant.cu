@@ -157,8 +157,8 @@ __global__ void __launch_bounds__(256, 3) prologue_quant_kernel(PrologueArgs p, 
   const __nv_bfloat16* qi = static_cast<const __nv_bfloat16*>(p.q_in) + h * kHeadDim + lane16 * 8;
   const __nv_bfloat16* ki = static_cast<const __nv_bfloat16*>(p.k_in) + h * kHeadDim + lane16 * 8;
   const __nv_bfloat16* vi = static_cast<const __nv_bfloat16*>(a.v) + h * kHeadDim + lane16 * 8;
-  const float* gq = p.gain_q + h * p.gain_head_stride;
-  const float* gk = p.gain_k + h * p.gain_head_stride;
+  const float* gqp = p.gain_q + h * p.gain_head_stride;
+  const float* gkp = p.gain_k + h * p.gain_head_stride;
   uint8_t* q8 = static_cast<uint8_t*>(a.q8) + h * kHeadDim + lane16 * 8;
   // rows of this lane group: tokens te.x + tl0 + 16 u for u < n_rows
   const int rem = te.y - te.x - tl0;
@@ -191,6 +191,8 @@ __global__ void __launch_bounds__(256, 3) prologue_quant_kernel(PrologueArgs p, 
       qkn::load_cs16(p.rope, valid ? t : (int64_t)te.x, lane16, c, s);
       float x[8];
       qkn::unpack8(kraw[i], x);
+      float gk[8];
+      qkn::load_gain16(gkp, lane16, gk);
       qkn::norm_rope16(x, gk, c, s, lane16, mask, p.eps);
       const uint4 kb = qkn::pack8(x);
       k_tile[tl0 + 16 * u][lane16] = kb;
@@ -198,6 +200,8 @@ __global__ void __launch_bounds__(256, 3) prologue_quant_kernel(PrologueArgs p, 
 #pragma unroll
       for (int e = 0; e < 8; ++e) kmax = fmaxf(kmax, fabsf(x[e]));
       qkn::unpack8(qraw[i], x);
+      float gq[8];
+      qkn::load_gain16(gqp, lane16, gq);
       qkn::norm_rope16(x, gq, c, s, lane16, mask, p.eps);
       qkn::unpack8(qkn::pack8(x), x);
       float m = 0.f;

@@ -27,7 +27,7 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kRowsPerBlock = kThreads / 16;
 
-__global__ void __launch_bounds__(kThreads) qk_prologue_kernel(PrologueArgs a) {
+__global__ void __launch_bounds__(kThreads, 4) qk_prologue_kernel(PrologueArgs a) {
   const int lane16 = threadIdx.x & 15;
   const unsigned mask = 0xffffu << (threadIdx.x & 16);
   const int64_t n_rows = a.S * a.H;
@@ -37,11 +37,17 @@ __global__ void __launch_bounds__(kThreads) qk_prologue_kernel(PrologueArgs a) {
   __nv_bfloat16* qo = static_cast<__nv_bfloat16*>(a.q_out);
   __nv_bfloat16* ko = static_cast<__nv_bfloat16*>(a.k_out);
   const bool with_q = a.q_in != nullptr;  // k only when q is handled by the forward
+  const int64_t row0 = (int64_t)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 4);
+  if (row0 >= n_rows) return;  // the whole 16-lane group, which alone shuffles together
+  // The launcher makes the grid-stride step a multiple of H (or gives each
+  // lane group one row), so a lane group keeps one head and loads its gains once.
+  const int head = (int)(row0 % a.H);
+  float gk[8], gq[8];
+  qkn::load_gain16(a.gain_k + head * a.gain_head_stride, lane16, gk);
+  if (with_q) qkn::load_gain16(a.gain_q + head * a.gain_head_stride, lane16, gq);
 #pragma unroll 1
-  for (int64_t row = (int64_t)blockIdx.x * kRowsPerBlock + (threadIdx.x >> 4); row < n_rows;
-       row += step) {
+  for (int64_t row = row0; row < n_rows; row += step) {
     const int64_t tok = row / a.H;
-    const int head = (int)(row - tok * a.H);
     const int64_t in_off = tok * a.in_stride + head * kHeadDim + lane16 * 8;
     const uint4 kraw = __ldcs(reinterpret_cast<const uint4*>(ki + in_off));
     const uint4 qraw = with_q ? __ldcs(reinterpret_cast<const uint4*>(qi + in_off)) : make_uint4(0, 0, 0, 0);
@@ -49,13 +55,13 @@ __global__ void __launch_bounds__(kThreads) qk_prologue_kernel(PrologueArgs a) {
     qkn::load_cs16(a.rope, tok, lane16, c, s);
     float xk[8];
     qkn::unpack8(kraw, xk);
-    qkn::norm_rope16(xk, a.gain_k + head * a.gain_head_stride, c, s, lane16, mask, a.eps);
+    qkn::norm_rope16(xk, gk, c, s, lane16, mask, a.eps);
     const int64_t out_off = tok * a.out_stride + head * kHeadDim + lane16 * 8;
     __stcs(reinterpret_cast<uint4*>(ko + out_off), qkn::pack8(xk));
     if (with_q) {
       float xq[8];
       qkn::unpack8(qraw, xq);
-      qkn::norm_rope16(xq, a.gain_q + head * a.gain_head_stride, c, s, lane16, mask, a.eps);
+      qkn::norm_rope16(xq, gq, c, s, lane16, mask, a.eps);
       __stcs(reinterpret_cast<uint4*>(qo + out_off), qkn::pack8(xq));
     }
   }
@@ -66,12 +72,26 @@ __global__ void __launch_bounds__(kThreads) qk_prologue_kernel(PrologueArgs a) {
 cudaError_t launch_qk_prologue(const PrologueArgs& a, int num_sms, cudaStream_t stream) {
   const int64_t n_rows = a.S * a.H;
   if (n_rows == 0) return cudaSuccess;
-  // 8 blocks of 256 threads per SM (at 64 registers, 4 of them are resident at
-  // a time; the grid-stride loop keeps the rest queued behind), or fewer
-  // when there is less work.  A variant with two rows of loads in flight per
-  // lane group and a single resident wave measured slower (3.7 vs 4.4 TB/s).
+  // 8 blocks of 256 threads per SM (capped at 64 registers, 4 of them are
+  // resident at a time; the grid-stride loop keeps the rest queued behind), or
+  // fewer when there is less work.  A variant with two rows of loads in flight
+  // per lane group and a single resident wave measured slower (3.7 vs 4.4
+  // TB/s); hoisting the gains at 72 registers (3 blocks resident) measured 112
+  // instead of 94 us.
+  // A full grid is rounded down to a multiple of H / gcd(16, H) blocks, so that
+  // the grid-stride step (16 rows per block) is a multiple of H and a lane
+  // group's head stays fixed.
   const int64_t want = (n_rows + kRowsPerBlock - 1) / kRowsPerBlock;
-  const int64_t full = (int64_t)num_sms * 8;
+  int64_t full = (int64_t)num_sms * 8;
+  int64_t g16 = kRowsPerBlock, h = a.H;
+  while (h != 0) {
+    const int64_t t = g16 % h;
+    g16 = h;
+    h = t;
+  }
+  const int64_t unit = a.H / g16;  // g16 = gcd(16, H)
+  full = full / unit * unit;
+  if (full < unit) full = unit;
   const int grid = (int)(want < full ? want : full);
   qk_prologue_kernel<<<grid, kThreads, 0, stream>>>(a);
   return cudaGetLastError();

@@ -99,18 +99,15 @@ __device__ __forceinline__ void load_cs16(const float2* rope, int64_t tok, int l
 }
 
 // One row spread over 16 lanes (lane16 = lane within its group of 16, mask =
-// the group's lanes): normalise x (this lane's 8 dims), apply the gain and
-// the rotation.  c, s: cos/sin of this lane's 8 angles (1, 0 for lanes 12..15).
-__device__ __forceinline__ void norm_rope16(float (&x)[8], const float* gain, const float (&c)[8],
-                                          const float (&s)[8], int lane16, unsigned mask,
-                                          float eps) {
+// the group's lanes): normalise x (this lane's 8 dims), apply the gain g (this
+// lane's 8 gains) and the rotation.  c, s: cos/sin of this lane's 8 angles (1,
+// 0 for lanes 12..15).
+__device__ __forceinline__ void norm_rope16(float (&x)[8], const float (&g)[8], const float (&c)[8],
+                                            const float (&s)[8], int lane16, unsigned mask, float eps) {
   float ss = chunk_ss(x);
 #pragma unroll
   for (int off = 8; off > 0; off >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(mask, ss, off, 16));
   const float r = inv_rms(ss, eps);
-  const float4 g0 = __ldg(reinterpret_cast<const float4*>(gain + lane16 * 8));
-  const float4 g1 = __ldg(reinterpret_cast<const float4*>(gain + lane16 * 8 + 4));
-  const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
   float y[8];
 #pragma unroll
   for (int e = 0; e < 8; ++e) y[e] = scale_gain(x[e], r, g[e]);
@@ -128,6 +125,14 @@ __device__ __forceinline__ void norm_rope16(float (&x)[8], const float* gain, co
 #pragma unroll
     for (int e = 0; e < 8; ++e) x[e] = y[e];
   }
+}
+
+// The 8 gains of lane lane16 (gain: the head's 128 gains, 16-byte aligned).
+__device__ __forceinline__ void load_gain16(const float* gain, int lane16, float (&g)[8]) {
+  const float4 g0 = __ldg(reinterpret_cast<const float4*>(gain + lane16 * 8));
+  const float4 g1 = __ldg(reinterpret_cast<const float4*>(gain + lane16 * 8 + 4));
+  g[0] = g0.x; g[1] = g0.y; g[2] = g0.z; g[3] = g0.w;
+  g[4] = g1.x; g[5] = g1.y; g[6] = g1.z; g[7] = g1.w;
 }
 
 }  // namespace qkn

@@ -159,3 +159,25 @@ def test_prologue_kernel_paths(lib, Hh, k_only):
             ko2 = torch.empty_like(k)
             _run(p, None, k, None, ko2, None, gk)
             assert torch.equal(ko2.view(torch.int16), ko.view(torch.int16))
+
+
+@pytest.mark.parametrize("Hh,S", [(21, 4096), (56, 1024), (16, 4096)])
+def test_prologue_per_head_gains_full_grid(lib, Hh, S):
+    # More rows than one pass of the grid (8 blocks of 16 rows per SM), so every
+    # 16-lane group runs several rows: the grid-stride step must keep each
+    # group on one head, whose gains it loads once (21, 56 and 16 heads give
+    # grid units of 21, 7 and 1 blocks).
+    docs = [[(S // 64, 8, 8, (0.0, 0.0, 0.0), (1.0, 1.0, 1.0))]]
+    t = random_tensors(S, Hh, 97 + Hh)
+    rng = np.random.default_rng(Hh)
+    gq = (1 + 0.3 * rng.standard_normal((Hh, 128))).astype(np.float32)
+    gk = (1 + 0.3 * rng.standard_normal((Hh, 128))).astype(np.float32)
+    with H.Plan(docs, Hh) as p:
+        q = bf16_to_torch(t.q).view(S, Hh * 128)
+        k = bf16_to_torch(t.k).view(S, Hh * 128)
+        qo, ko = torch.empty_like(q), torch.empty_like(k)
+        _run(p, q, k, qo, ko, torch.from_numpy(gq).cuda(), torch.from_numpy(gk).cuda(), ghs=128)
+        yq = torch_bf16_to_f64(qo).reshape(S, Hh, 128)
+        yk = torch_bf16_to_f64(ko).reshape(S, Hh, 128)
+    check_prologue(yq, _oracle(docs, t.q, gq), f"per-head q gains, {Hh} heads")
+    check_prologue(yk, _oracle(docs, t.k, gk), f"per-head k gains, {Hh} heads")
