@@ -716,6 +716,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     const float sl2 = a.scale_log2;
     __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.o);
+    // 32-byte output stores when every row start is 32-byte aligned
+    const bool o_wide = (reinterpret_cast<uintptr_t>(a.o) & 31u) == 0 && (a.o_stride & 15) == 0;
     for (int u = u_begin; ok && u < u_end; ++u) {
       const UnitGeom g = unit_geom(a.units, u);
       const uint32_t t_unit = t0;
@@ -856,8 +858,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (g.part >= 0) {
         // A piece of a unit split along the keys: unnormalised O row, its
         // reference max (log2 units) and sum, for the merge pass.
+        // (the partial buffer is a device allocation: its 512-byte rows are 32-byte aligned)
         const size_t slot = (size_t)g.part * kUnitRows + local;
-        float4* dst = reinterpret_cast<float4*>(a.part_o + slot * kHeadDim);
+        float* dst = a.part_o + slot * kHeadDim;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t ov[32];
@@ -866,9 +869,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if constexpr (kFp8) scale_by_channel(ov, a.sv + g.head * kHeadDim + c * 32);
           if (valid) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              dst[c * 8 + e] = make_float4(__uint_as_float(ov[4 * e]), __uint_as_float(ov[4 * e + 1]),
-                                           __uint_as_float(ov[4 * e + 2]), __uint_as_float(ov[4 * e + 3]));
+            for (int e = 0; e < 4; ++e)
+              dev::st_global_v8(dst + c * 32 + e * 8, ov[8 * e], ov[8 * e + 1], ov[8 * e + 2], ov[8 * e + 3],
+                                ov[8 * e + 4], ov[8 * e + 5], ov[8 * e + 6], ov[8 * e + 7]);
           }
         }
         if (valid) a.part_ml[slot] = make_float2(m_used, l);
@@ -883,14 +886,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         dev::tmem_wait_ld();
         if constexpr (kFp8) scale_by_channel(ov, a.sv + g.head * kHeadDim + c * 32);
         if (valid) {
+          uint32_t w[16];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            uint4 w;
-            w.x = dev::pack_bf16x2(__uint_as_float(ov[8 * e + 0]) * inv, __uint_as_float(ov[8 * e + 1]) * inv);
-            w.y = dev::pack_bf16x2(__uint_as_float(ov[8 * e + 2]) * inv, __uint_as_float(ov[8 * e + 3]) * inv);
-            w.z = dev::pack_bf16x2(__uint_as_float(ov[8 * e + 4]) * inv, __uint_as_float(ov[8 * e + 5]) * inv);
-            w.w = dev::pack_bf16x2(__uint_as_float(ov[8 * e + 6]) * inv, __uint_as_float(ov[8 * e + 7]) * inv);
-            *reinterpret_cast<uint4*>(dst + c * 32 + e * 8) = w;
+          for (int e = 0; e < 16; ++e)
+            w[e] = dev::pack_bf16x2(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
+          if (o_wide) {  // rows and chunks 32-byte aligned: two 32-byte stores per chunk
+            dev::st_global_v8(dst + c * 32, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+            dev::st_global_v8(dst + c * 32 + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              *reinterpret_cast<uint4*>(dst + c * 32 + e * 8) = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
           }
         }
       }

@@ -195,3 +195,30 @@ def test_running_max_jump_rescales_o(lib, col):
     share = w[:, :, jump] / w.sum(axis=2)
     assert 0.2 < share.min() and share.max() < 0.8
     check_attention(o_gpu, o_ref, lse.cpu().numpy(), lse_ref, f"running max jump at column {col}")
+
+
+@pytest.mark.parametrize("offset,pad", [(8, 0), (0, 8), (8, 8)])
+def test_output_alignments_are_byte_identical(lib, offset, pad):
+    # o starting 16 bytes past a 32-byte boundary and/or a row stride that is a
+    # multiple of 8 but not of 16 elements: the epilogue's 16-byte stores
+    # instead of its 32-byte ones, same bytes.  Ragged documents and a split
+    # last wave (units that write partial results) included.
+    lens = [1000, 3, 513, 129, 1]
+    Hh = 3
+    S, W = sum(lens), Hh * 128
+    t = random_tensors(S, Hh, seed=61)
+    r0 = run_product(docs_1d(lens), Hh, t)
+    dev = torch.device("cuda")
+    with H.Plan(docs_1d(lens), Hh) as p:
+        q, k, v = (bf16_to_torch(x).view(S, W) for x in (t.q, t.k, t.v))
+        gq, gk = torch.from_numpy(t.gain_q).to(dev), torch.from_numpy(t.gain_k).to(dev)
+        qh, kh = torch.empty_like(q), torch.empty_like(k)
+        H.h3attn_qk_prologue(p.handle, q, k, qh, kh, gq, gk, 1e-6)
+        stride = W + pad
+        base = torch.zeros(S * stride + offset + 16, dtype=torch.bfloat16, device=dev)
+        assert base.data_ptr() % 32 == 0
+        o = base[offset:offset + S * stride].view(S, stride)[:, :W]
+        H.h3attn_forward(p.handle, qh, kh, v, o, 1.0 / np.sqrt(128.0), None, o_row_stride=stride)
+        H.h3attn_get_device_error(p.handle)
+        got = o.contiguous().view(torch.int16).cpu().numpy().reshape(S, Hh, 128)
+    assert np.array_equal(got, np.asarray(r0.o_bits).reshape(S, Hh, 128))
