@@ -36,7 +36,9 @@
 // While one softmax group works on its tile, the tensor cores run the other
 // tile's MMAs (two-tile ping-pong).  A unit only visits its own document's key
 // tiles; keys past the document end in the last tile are masked to -inf, rows
-// past it are never stored.
+// past it are never stored.  Each pair runs its own range of the work list
+// (placed on the host longest-processing-time first); in bf16 the next unit's
+// first QKs are issued during the current unit's last key tile.
 //
 // TMEM columns (each CTA): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512);
 // P_s is bf16 packed two per column in the first 64 columns of S_s.
