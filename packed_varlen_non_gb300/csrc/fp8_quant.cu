@@ -292,32 +292,44 @@ __global__ void __launch_bounds__(128) vmax_kernel(Fp8QuantArgs a) {
 // tile, head) writes v8t[h][c][vb .. vb + n) for all 128 channels, where the
 // tile's n <= 128 keys start at vb in the transposed layout (every document
 // starts on a 16-key boundary); a document's last tile also zero-fills up to
-// the next boundary.
+// the next boundary.  Thread i codes 4 consecutive keys (4 (i%32) ..) of 16
+// channels (16 (i/32) ..) and packs each channel's 4 codes into one 32-bit
+// word, so a warp stores 32 consecutive words of one channel row.
 __global__ void __launch_bounds__(256) vquant_kernel(Fp8QuantArgs a) {
-  __shared__ __align__(16) uint8_t tile[128][128 + 16];
+  constexpr int kRowWords = 36;  // 32 words of keys + 4 of padding (rows stay 16-byte aligned)
+  __shared__ __align__(16) uint32_t tile[128 * kRowWords];
   __shared__ float rc[128];  // per-channel 448 / amax
   const int4 te = a.tiles[blockIdx.x];
   const int h = blockIdx.y;
   const int n = te.y - te.x;
-  const int tl = threadIdx.x >> 1, c0 = (threadIdx.x & 1) * 64;
   if (threadIdx.x < 128)
     rc[threadIdx.x] = fp8_recip(__uint_as_float(reinterpret_cast<const uint32_t*>(a.sv)[h * kHeadDim + threadIdx.x]));
   __syncthreads();
-  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.v) + (int64_t)(te.x + tl) * a.stride + h * kHeadDim + c0;
-#pragma unroll 1
-  for (int c = 0; c < 64; c += 8) {
-    float f[8];
-    if (tl < n) {
-      unpack8(__ldg(reinterpret_cast<const uint4*>(x + c)), f);
-    } else {
+  const int tq = threadIdx.x & 31, cg = threadIdx.x >> 5;
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.v) + (int64_t)te.x * a.stride + h * kHeadDim + cg * 16;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) f[e] = 0.f;
+  for (int half = 0; half < 2; ++half) {
+    const int ch0 = cg * 16 + half * 8;
+    uint32_t pr[4][4];  // [key][channel pair]: two codes, the even channel's in the low byte
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = 4 * tq + i;
+      float f[8];
+      if (t < n) {
+        unpack8(__ldg(reinterpret_cast<const uint4*>(x + (int64_t)t * a.stride + half * 8)), f);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = 0.f;
+      }
+#pragma unroll
+      for (int p = 0; p < 4; ++p)
+        pr[i][p] = e4m3x2(__fmul_rn(f[2 * p], rc[ch0 + 2 * p]), __fmul_rn(f[2 * p + 1], rc[ch0 + 2 * p + 1]));
     }
 #pragma unroll
-    for (int e = 0; e < 8; e += 2) {
-      const uint32_t two = e4m3x2(__fmul_rn(f[e], rc[c0 + c + e]), __fmul_rn(f[e + 1], rc[c0 + c + e + 1]));
-      tile[c0 + c + e][tl] = (uint8_t)(two & 0xff);
-      tile[c0 + c + e + 1][tl] = (uint8_t)(two >> 8);
+    for (int p = 0; p < 4; ++p) {
+      const uint32_t lo = pr[0][p] | (pr[1][p] << 16), hi = pr[2][p] | (pr[3][p] << 16);
+      tile[(ch0 + 2 * p) * kRowWords + tq] = __byte_perm(lo, hi, 0x6420);      // even channel, keys 0..3
+      tile[(ch0 + 2 * p + 1) * kRowWords + tq] = __byte_perm(lo, hi, 0x7531);  // odd channel
     }
   }
   __syncthreads();
@@ -328,7 +340,7 @@ __global__ void __launch_bounds__(256) vquant_kernel(Fp8QuantArgs a) {
 #pragma unroll
   for (int p = 0; p < 4; ++p)
     if (k0 + p * 16 < n16)
-      *reinterpret_cast<uint4*>(out + p * 16) = *reinterpret_cast<const uint4*>(&tile[ch][k0 + p * 16]);
+      *reinterpret_cast<uint4*>(out + p * 16) = *reinterpret_cast<const uint4*>(&tile[ch * kRowWords + k0 / 4 + 4 * p]);
 }
 
 __global__ void vscale_kernel(Fp8QuantArgs a) {
