@@ -197,7 +197,9 @@ h3attn_status h3attn_fp8_quantize(h3attn_plan_t plan, const void* q_hat, const v
                                   int64_t qkv_row_stride, void* q8, void* k8, void* v8t, float* sq, float* sk,
                                   float* sv, void* cuda_stream);
 
-/* The q/k prologue and the FP8 quantisation in one call, for the FP8 step:
+/* The q/k prologue and the FP8 quantisation in one call, for the FP8 step
+ * ([SPARK] "What this config does": the fused Q RMSNorm + rot96 kernel also
+ * quantises Q for the low-precision attention; here q and k, to e4m3):
  * the same codes and scales as h3attn_qk_prologue (gains and eps as there)
  * followed by h3attn_fp8_quantize on its bf16 outputs and on v, without
  * q-hat and k-hat ever being written.  q_in, k_in, v: bf16 [S,H,128] with
