@@ -26,3 +26,15 @@ def test_reference_arm_prints_one_contract_line(capsys):
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
     # the value is the sampled rows' algorithmic FLOPs over the sampled time
     assert rec["value"] * 1e12 * rec["ms_per_step"] * 1e-3 > 4 * 128 * 20423 * 512
+
+
+def test_kernel_code_hash_ignores_comments_only(tmp_path):
+    # the recorded DRAM traffic stays valid across comment edits, not code edits
+    a = tmp_path / "a.cu"
+    b = tmp_path / "b.cu"
+    c = tmp_path / "c.cu"
+    a.write_text("// header\n__global__ void k(int* p) {\n  p[0] = 1;  // store\n}\n")
+    b.write_text("// a different header\n\n__global__ void k(int* p) {\n  p[0] = 1;\n}\n")
+    c.write_text("// header\n__global__ void k(int* p) {\n  p[0] = 2;  // store\n}\n")
+    assert bench.kernel_code_hash(str(a)) == bench.kernel_code_hash(str(b))
+    assert bench.kernel_code_hash(str(a)) != bench.kernel_code_hash(str(c))
