@@ -69,6 +69,16 @@ def test_compute_calls_reject_a_null_plan(lib):
                                                 stream=0)) == H.H3ATTN_EINVAL
     assert _status(lambda: H.h3attn_get_device_error(None, stream=0)) == H.H3ATTN_EINVAL
     assert _status(lambda: H.h3attn_plan_info(None)) == H.H3ATTN_EINVAL
+    assert _status(lambda: H.h3attn_forward_fused_q(None, 16, 16, 16, 16, 16, 0.1, qkv_row_stride=128,
+                                                    o_row_stride=128, stream=0)) == H.H3ATTN_EINVAL
+    assert _status(lambda: H.h3attn_fp8_quantize(None, 16, 16, 16, 16, 16, 16, 16, 16, 16, qkv_row_stride=128,
+                                                 stream=0)) == H.H3ATTN_EINVAL
+    assert _status(lambda: H.h3attn_qk_prologue_fp8(None, 16, 16, 16, 16, 16, 1e-6, 16, 16, 16, 16, 16, 16,
+                                                    qkv_row_stride=128, stream=0)) == H.H3ATTN_EINVAL
+    assert _status(lambda: H.h3attn_forward_fp8(None, 16, 16, 16, 16, 16, 16, 16, 0.1, o_row_stride=128,
+                                                stream=0)) == H.H3ATTN_EINVAL
+    assert _status(lambda: H.h3attn_plan_fp8_v_keys(None)) == H.H3ATTN_EINVAL
+    assert _status(lambda: H.h3attn_plan_forward_kernels(None)) == H.H3ATTN_EINVAL
     H.h3attn_plan_destroy(None)  # accepted and ignored
 
 
