@@ -38,7 +38,12 @@
  *   - Functions never throw across the boundary.  Arguments are validated
  *     before anything is launched; on failure nothing is launched, the
  *     status says why, and h3attn_last_error() holds a message.
- *   - A plan is used from one host thread at a time.
+ *   - A plan is used from one host thread at a time, and the calls that use
+ *     one plan must not overlap on the GPU: every forward issued with a plan
+ *     writes its partial-result buffers (the pieces of a split last wave) and
+ *     its device error word, so two forwards with the same plan running at
+ *     once on two streams race on them.  Issue them on one stream, order the
+ *     streams with events, or give each concurrent stream its own plan.
  */
 #ifndef H3ATTN_H_
 #define H3ATTN_H_
@@ -294,10 +299,16 @@ h3attn_status h3attn_forward_fp8(h3attn_plan_t plan, const void* q8, const void*
  * on a device looks up the array's device address (cudaGetSymbolAddress) with
  * that device current; make that first call before any stream capture.  All
  * calls share the array and it keeps the last call's contents: the work list
- * is rewritten and the error word cleared on every call, and calls that
- * overlap on the GPU (e.g. on two streams at once) race on it.  A bounded-wait
- * timeout inside the kernel invalidates the output but is not reported here
- * (there is no plan to hold it); use h3attn_forward where that matters. */
+ * is rewritten and the error word cleared on every call.  Calls from several
+ * host threads on one stream are safe: each call enqueues its copy of the
+ * work list and its kernel under one lock, so they run in that order.  Calls
+ * that overlap on the GPU (on two streams at once) race on the array.  A
+ * bounded-wait timeout inside the kernel invalidates the output but is not
+ * reported here (there is no plan to hold it); use h3attn_forward where that
+ * matters.  Unlike h3attn_forward, this path never splits the last round of
+ * work units along the keys (that needs partial buffers), so its output can
+ * differ from h3attn_forward's in the last bits while both stay within the
+ * same tolerance of exact attention. */
 h3attn_status h3attn_forward_noalloc(const int32_t* cu_seqlens, int32_t n_docs, int32_t num_heads,
                                      const void* q, const void* k, const void* v,
                                      int64_t qkv_row_stride, void* o, int64_t o_row_stride,

@@ -56,7 +56,8 @@ cudaError_t scratch_on_device(int dev, int4** out) {
 
 // Host staging of the work list (pageable; cudaMemcpyAsync from pageable
 // memory returns once the bytes are staged, so the buffer can be refilled by
-// the next call).  Guarded by a mutex so host threads do not interleave.
+// the next call).  Guarded by a mutex held until the kernel is enqueued, so
+// host threads do not interleave their copies and launches.
 std::mutex g_stage_mutex;
 WorkUnit g_stage[kNoAllocMaxUnits];
 int32_t g_order[kNoAllocMaxUnits];
@@ -139,10 +140,13 @@ extern "C" h3attn_status h3attn_forward_noalloc(const int32_t* cu_seqlens, int32
     return fail(H3ATTN_ECUDA, "cudaGetSymbolAddress: %s", cudaGetErrorString(e));
 
   cudaStream_t st = static_cast<cudaStream_t>(cuda_stream);
+  // The lock is held from staging the work list until the kernel is enqueued:
+  // two host threads sharing a stream then enqueue (copy, kernel) pairs that
+  // never interleave, so each kernel reads its own list.
+  std::lock_guard<std::mutex> lock(g_stage_mutex);
   int32_t n_pairs = 0;
   {
     // Same work-list order as a plan: longest documents first, then head, then query tile.
-    std::lock_guard<std::mutex> lock(g_stage_mutex);
     // (each document contributes at least one unit, so n_docs <= n_units <= the buffer size)
     for (int32_t d = 0; d < n_docs; ++d) g_order[d] = d;
     std::sort(g_order, g_order + n_docs, [cu_seqlens](int32_t x, int32_t y) {
