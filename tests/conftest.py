@@ -19,3 +19,20 @@ def lib():
     from packed_varlen_non_gb300 import build, h3attn
     build.ensure_built()
     return h3attn
+
+
+# Full-output parity figures (max / mean abs error over every element), printed
+# in the terminal summary so that they show even in a quiet run.
+_PARITY_LINES = []
+
+
+@pytest.fixture
+def parity_report():
+    return _PARITY_LINES.append
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    if _PARITY_LINES:
+        terminalreporter.write_sep("-", "full-output parity against the fp64 oracle")
+        for line in _PARITY_LINES:
+            terminalreporter.write_line(line)

@@ -92,6 +92,7 @@ def run_product(docs, num_heads, t: synth.Tensors, eps=1e-6, scale=None, stream=
         r.o = torch_bf16_to_f64(o).reshape(S, num_heads, 128)
         r.o_bits = o.view(torch.int16).cpu().numpy()
         r.k_bits = k_hat.view(torch.int16).cpu().numpy()
+        r.q_bits = None if fused_q else q_hat.view(torch.int16).cpu().numpy()
         r.lse = lse.cpu().numpy() if want_lse else None
         if keep_device:
             r.dev = dict(q_hat=q_hat, k_hat=k_hat, v=v, o=o)

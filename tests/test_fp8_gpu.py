@@ -140,15 +140,6 @@ def test_fp8_forward_within_bound(lib, lens, Hh):
     check_fp8_forward(lens, Hh, t, what=str(lens))
 
 
-def test_fp8_forward_ref2va_sampled(lib):
-    from tests.gpu_cases import sample_rows
-    w = synth.config(3)
-    t = synth.make_tensors(w)
-    cu = np.concatenate([[0], np.cumsum(w.doc_lengths)])
-    rows = sample_rows(cu, per_edge=8, interior=24, seed=3)
-    check_fp8_forward(list(w.doc_lengths), w.num_heads, t, rows=rows, what="Ref2VA sampled")
-
-
 def test_fp8_rejects_bad_arguments(lib):
     lens, Hh = [300, 40], 2
     S = sum(lens)
