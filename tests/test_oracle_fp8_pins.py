@@ -68,10 +68,8 @@ def test_quantisers_closed_forms():
     assert np.array_equal(s, (np.abs(x).max(axis=2) / np.float32(448)).T)
     top = np.abs(fp8.e4m3_decode(codes)).max(axis=2)
     assert np.all(np.abs(top - 448) <= 16)
-    # codes are e4m3(x * (448 / amax)) in fp32; dequantised values within half a quantum
-    # (relative 2^-4) of the input, or 2^-10 s absolute, up to the fp32 roundings of r and s
-    r = np.float32(448) / np.abs(x).max(axis=2)
-    assert np.array_equal(codes, fp8.e4m3_encode((x * r[:, :, None]).astype(np.float32)))
+    # every dequantised value within half a quantum (relative 2^-4, or 2^-10 s in
+    # the subnormal range) of its input, up to the fp32 roundings of r, s and x * r
     deq = fp8.e4m3_decode(codes) * s.T[:, :, None]
     err = np.abs(deq - x)
     assert np.all(err <= (2.0 ** -4 + 2.0 ** -20) * np.abs(x) + 2.0 ** -10 * s.T[:, :, None] + 1e-12)
@@ -86,6 +84,80 @@ def test_quantisers_closed_forms():
     z = x.copy(); z[5, 1] = 0
     c2, s2 = fp8.quantize_rows(z)
     assert s2[1, 5] == 1.0 and not c2[5, 1].any()
+
+
+def _clear_of_boundaries(y):
+    """Elements whose magnitude is more than one fp32 ulp away from every
+    e4m3 rounding boundary (the midpoints between neighbouring finite
+    magnitudes): there fp32 rounding of the product cannot change the code."""
+    mags = np.unique(np.abs(fp8.e4m3_decode(FINITE)))
+    mids = (mags[:-1] + mags[1:]) / 2
+    a = np.abs(y)
+    i = np.searchsorted(mids, a)
+    lo = mids[np.clip(i - 1, 0, mids.size - 1)]
+    hi = mids[np.clip(i, 0, mids.size - 1)]
+    dist = np.minimum(np.abs(a - lo), np.abs(a - hi))
+    return dist > np.spacing(a.astype(np.float32)).astype(np.float64)
+
+
+def test_row_codes_are_the_nearest_codes_of_the_exact_product():
+    # Fixed by the format alone, not by the oracle's formula: with amax the
+    # row's largest magnitude, each code is the e4m3 value nearest to the
+    # exact product x * 448 / amax (brute-force search over all finite codes),
+    # wherever that product is more than one fp32 ulp from a rounding
+    # boundary; there the dequantised value is within half a quantum of x:
+    # 2^-4 |x| (normal codes) or 2^-10 s (subnormal codes), without widening.
+    rng = np.random.default_rng(11)
+    S, H, D = 96, 2, 128
+    x = (rng.standard_normal((S, H, D)) * np.exp(rng.uniform(-3, 3, (S, H, 1)))).astype(np.float32)
+    x[3, 0, 7] = 0.0
+    codes, s = fp8.quantize_rows(x)
+    amax = np.abs(x).astype(np.float64).max(axis=2)
+    y = x.astype(np.float64) * (448.0 / amax)[:, :, None]
+    clear = _clear_of_boundaries(y)
+    assert clear.mean() > 0.99
+    want = _brute(y[clear])
+    assert np.array_equal(fp8.e4m3_decode(codes[clear]), fp8.e4m3_decode(want))
+    deq = fp8.e4m3_decode(codes) * s.T[:, :, None].astype(np.float64)
+    bound = np.maximum(2.0 ** -4 * np.abs(x), 2.0 ** -10 * s.T[:, :, None])
+    assert np.all(np.abs(deq - x)[clear] <= bound[clear])
+
+
+def test_key_tile_and_channel_codes_are_the_nearest_codes_of_the_exact_product():
+    # the same pin for the per-key-tile and per-channel quantisers
+    rng = np.random.default_rng(12)
+    S, H, D = 300, 2, 32
+    x = rng.standard_normal((S, H, D)).astype(np.float32) * np.float32(3.0)
+    cu = np.array([0, 130, 131, 300])
+    k8, sk = fp8.quantize_key_tiles(x, cu)
+    y = np.zeros(x.shape)
+    for a, b in fp8.key_tiles(cu):
+        amax = np.abs(x[a:b]).astype(np.float64).max(axis=(0, 2))
+        y[a:b] = x[a:b].astype(np.float64) * (448.0 / amax)[None, :, None]
+    clear = _clear_of_boundaries(y)
+    assert np.array_equal(fp8.e4m3_decode(k8[clear]), fp8.e4m3_decode(_brute(y[clear])))
+    v8, sv = fp8.quantize_channels(x)
+    yv = x.astype(np.float64) * (448.0 / np.abs(x).astype(np.float64).max(axis=0))[None]
+    clear = _clear_of_boundaries(yv)
+    assert np.array_equal(fp8.e4m3_decode(v8[clear]), fp8.e4m3_decode(_brute(yv[clear])))
+
+
+def test_row_pin_catches_a_truncating_encoder(monkeypatch):
+    # a plausible mistake -- rounding the product toward zero instead of to
+    # nearest -- fails the nearest-code pin
+    real = fp8.e4m3_encode
+
+    def truncating(y):
+        y = np.asarray(y, dtype=np.float64)
+        c = real(y)
+        v = fp8.e4m3_decode(c)
+        over = np.abs(v) > np.abs(y)
+        down = np.where(c & 0x7F, c - 1, c).astype(np.uint8)
+        return np.where(over, down, c).astype(np.uint8)
+
+    monkeypatch.setattr(fp8, "e4m3_encode", truncating)
+    with pytest.raises(AssertionError):
+        test_row_codes_are_the_nearest_codes_of_the_exact_product()
 
 
 def test_error_bound_covers_p_rounding():
