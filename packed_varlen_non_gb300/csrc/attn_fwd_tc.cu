@@ -24,46 +24,65 @@
 //                in place when asked (RMSNorm with gain, rot96 rotation) and
 //                reports the tile ready to the even CTA.  Q tiles are double
 //                buffered, so the next unit's tiles are ready before it starts.
-//   warp 8       even CTA: MMA issuer for the pair, S_s = Q_s K_j^T and
-//                O_s += P_s V_j, fp32 accumulators in TMEM.  Both CTAs'
-//                warp 8 allocate the pair's TMEM together.
+//   warp 8       even CTA: MMA issuer for the pair, S = Q_s K^T and
+//                O_s += P V, fp32 accumulators in TMEM.  Both CTAs' warp 8
+//                allocate the pair's TMEM together.
 //   warps 0..3   softmax for query tile 0 of this CTA,
 //   warps 4..7   softmax for query tile 1: one thread per query row reads its
 //                S row from TMEM, keeps the running max and sum in registers,
 //                writes P as bf16 back into TMEM over its S columns, rescales
 //                its O row when the max has grown by more than 2^8, and at the
 //                end of the unit writes O / l and the log-sum-exp.
-// While one softmax group works on its tile, the tensor cores run the other
-// tile's MMAs (two-tile ping-pong).  A unit only visits its own document's key
-// tiles; keys past the document end in the last tile are masked to -inf, rows
-// past it are never stored.  Each pair runs its own range of the work list
-// (placed on the host longest-processing-time first); in bf16 the next unit's
-// first QKs are issued during the current unit's last key tile.
+// Each 128-key tile is taken in two halves of 64 keys, h = 0, 1, each with
+// its own 64 TMEM columns of S: per query tile the issuer runs PV of half h
+// of key tile j and then QK of half h of key tile j + 1 into the same
+// columns, so the softmax works on the other half while the tensor cores
+// compute the next S half -- a query tile's softmax does not wait for its own
+// PV and next QK.  Both query tiles and both halves interleave on the tensor
+// pipe (order per key tile: tile 0 half 0, tile 1 half 0, tile 0 half 1,
+// tile 1 half 1).  A unit only visits its own document's key tiles; keys past
+// the document end in the last tile are masked to -inf, rows past it are
+// never stored.  Each pair runs its own range of the work list (placed on the
+// host longest-processing-time first), and the next unit's first QKs are
+// issued during the current unit's last key tile.
 //
-// TMEM columns (each CTA): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512);
-// P_s is bf16 packed two per column in the first 64 columns of S_s.
+// Key halves: a CTA holds keys [64 rank, 64 rank + 64) of a tile; half h is
+// rows [32 h, 32 h + 32) of both CTAs' halves (the pair MMA takes B's first
+// 32 columns from the even CTA), so S column c of half h is key 32 h + c for
+// c < 32 and 64 + 32 h + (c - 32) for c >= 32; the PV of a half reads the
+// matching 16-key (bf16) or 32-key (FP8) chunks of V.
+//
+// TMEM columns (each CTA): S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512),
+// S_s half h at S_s + 64 h; P of a half is bf16 packed two per column in the
+// half's first 32 columns.
 //
 // Shared memory rows are 64 bf16 (128 B, 128-byte TMA swizzle).  Q tiles are
 // 128 rows x 128 dims (two 16 KB halves); a K half-tile is 64 keys x 128 dims
 // (two 8 KB halves), a V half-tile 128 keys x 64 dims (16 KB).  Q and K are
 // K-major operands; V is the MN-major B operand of the PV product.
 //
-// Barriers: completion of the pair's MMAs is multicast to both CTAs (S ready,
-// O ready, Q slots free).  The MMA-issuing thread paces the tensor cores, so
-// per key tile it only waits for P and commits S: its "P ready" barrier
-// counts one arrival per softmax warp of both CTAs, and softmax warp 0 of
-// each CTA arrives only once its CTA's next K/V group has landed; a softmax
-// thread that sees S of key tile t ready frees the ring slots of the group
-// holding K(t) (everything before that QK has completed).  Q tiles: the even
-// CTA's "Q ready" barrier counts one arrival from the Q warp of each CTA.
+// Barriers: completion of the pair's MMAs is multicast to both CTAs (S half
+// ready, PV done, Q slots free).  The MMA-issuing thread paces the tensor
+// cores, so per key-tile half it only waits for P and commits: its "P ready"
+// barrier of (query tile, half) counts one arrival per softmax warp of both
+// CTAs, and softmax warp 0 of each CTA reports half 0 only once its CTA's next
+// K/V group has landed; a softmax thread of the unit's last query tile that
+// sees S half 1 of key tile t ready frees the ring slots of the group holding
+// K(t) (everything before that QK has completed).  "PV done" of a query tile
+// and half completes once per unit, after the PV of that half in the unit's
+// last key tile: the epilogue waits for both halves.  A rescale of O first
+// waits for the other half's latest PV: through the S-ready of the QK issued
+// right after it, or "PV done" in the last key tile.  Q tiles:
+// the even CTA's "Q ready" barrier counts one arrival from the Q warp of each
+// CTA.
 //
 // FP8 variant (template argument kFp8, h3attn_forward_fp8): the same kernel
 // on e4m3 Q, K and transposed V (channel rows of keys, every document
 // starting on a 16-key boundary) with fp32 scales -- kind::f8f6f4 pair MMAs of
 // K = 32, 16 KB Q tiles and 8 KB half-tiles in 128-byte rows, P rounded to
-// e4m3 and stored four per TMEM column (first 32 columns of S), the q-row x
-// key-tile scale folded into the softmax's score multiplier, the per-channel
-// V scale applied to O in the epilogue.
+// e4m3 and stored four per TMEM column (first 16 columns of an S half), the
+// q-row x key-tile scale folded into the softmax's score multiplier, the
+// per-channel V scale applied to O in the epilogue.
 //
 // Every mbarrier wait is bounded: on expiry the CTA raises an abort flag,
 // records a timeout in the device error word, drains its own copies and MMAs
@@ -89,8 +108,8 @@ constexpr int kQWarp = 10;
 constexpr int kTileRows = 128;
 constexpr int kSlots = 6;                              // ring slots (16 KB each)
 constexpr int kGroups = kSlots / 2;                    // key/value groups in flight
-// barriers: q_full[4] q_empty[4] q_ready[4] kv_full[G] kv_empty[G] s_ready[2] p_ready[2] o_ready[2] drain
-constexpr int kNumBars = 12 + 2 * kGroups + 2 + 2 + 2 + 1;
+// barriers: q_full[4] q_empty[4] q_ready[4] kv_full[G] kv_empty[G] s_ready[2][2] p_ready[2][2] pv_done[2][2] drain
+constexpr int kNumBars = 12 + 2 * kGroups + 4 + 4 + 4 + 1;
 // Shared-memory layout: 2 buffers x 2 query tiles, then the ring.  bf16: a Q
 // tile is 128 rows x 128 dims in two 16 KB halves of 64 dims, a slot 16 KB;
 // fp8 (e4m3): a Q tile is one 16 KB block of 128-byte rows, a slot 8 KB.
@@ -113,12 +132,16 @@ constexpr float kRescaleThreshold = 8.0f;              // log2 units: rescale wh
 constexpr uint16_t kPairMask = 0x3;
 static_assert(kUnitRows == 4 * kTileRows, "a unit is two query tiles in each CTA of the pair");
 
-// Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, M = 256 (pair), N = 128.
-constexpr uint32_t kIdescBase = (1u << 4) | (1u << 7) | (1u << 10) | ((128u >> 3) << 17) | ((256u >> 4) << 24);
-constexpr uint32_t kIdescQK = kIdescBase;              // A, B K-major
-constexpr uint32_t kIdescPV = kIdescBase | (1u << 16);  // B (V) MN-major
-// kind::f8f6f4: e4m3 A and B (type code 0), fp32 accumulator, M = 256, N = 128, both K-major
-constexpr uint32_t kIdescF8 = (1u << 4) | ((128u >> 3) << 17) | ((256u >> 4) << 24);
+// Instruction descriptors, kind::f16: fp32 accumulator, bf16 A and B, M = 256 (pair).
+// QK: N = 64 keys (one half of a key tile), A and B K-major; PV: N = 128 dims,
+// B (V) MN-major.
+constexpr uint32_t kIdescBf16 = (1u << 4) | (1u << 7) | (1u << 10) | ((256u >> 4) << 24);
+constexpr uint32_t kIdescQK = kIdescBf16 | ((64u >> 3) << 17);
+constexpr uint32_t kIdescPV = kIdescBf16 | ((128u >> 3) << 17) | (1u << 16);
+// kind::f8f6f4: e4m3 A and B (type code 0), fp32 accumulator, M = 256, both
+// K-major; QK N = 64 keys, PV N = 128 dims
+constexpr uint32_t kIdescF8QK = (1u << 4) | ((64u >> 3) << 17) | ((256u >> 4) << 24);
+constexpr uint32_t kIdescF8PV = (1u << 4) | ((128u >> 3) << 17) | ((256u >> 4) << 24);
 
 // Q slot i = 2 * buffer + query tile; the unit with ordinal k (per pair) uses buffer k & 1.
 struct Bars {
@@ -128,10 +151,13 @@ struct Bars {
   __device__ uint32_t q_ready(int i) const { return base + 8 * (8 + i); }
   __device__ uint32_t kv_full(int i) const { return base + 8 * (12 + i); }
   __device__ uint32_t kv_empty(int i) const { return base + 8 * (12 + kGroups + i); }
-  __device__ uint32_t s_ready(int s) const { return base + 8 * (12 + 2 * kGroups + s); }
-  __device__ uint32_t p_ready(int s) const { return base + 8 * (14 + 2 * kGroups + s); }
-  __device__ uint32_t o_ready(int s) const { return base + 8 * (16 + 2 * kGroups + s); }
-  __device__ uint32_t drain() const { return base + 8 * (18 + 2 * kGroups); }
+  // S of key-tile half h of query tile s is in TMEM / P of it is in TMEM
+  __device__ uint32_t s_ready(int s, int h) const { return base + 8 * (12 + 2 * kGroups + 2 * s + h); }
+  __device__ uint32_t p_ready(int s, int h) const { return base + 8 * (16 + 2 * kGroups + 2 * s + h); }
+  // the PV of half h of query tile s in a unit's last key tile has completed
+  // (one phase per unit)
+  __device__ uint32_t pv_done(int s, int h) const { return base + 8 * (20 + 2 * kGroups + 2 * s + h); }
+  __device__ uint32_t drain() const { return base + 8 * (24 + 2 * kGroups); }
 };
 
 struct UnitGeom {
@@ -188,101 +214,122 @@ __device__ __forceinline__ uint32_t desc_lo(uint32_t addr, uint32_t lbo) {
   return ((addr >> 4) & 0x3FFFu) | ((lbo >> 4) << 16);
 }
 
-// S (TMEM, 128 x 128 fp32 in each CTA) = Q (smem, K-major) * K^T (smem, K-major,
-// 64 keys per CTA): 8 pair MMAs of K = 16 in one block.  Step kk reads Q at
-// +(kk/4) 16 KB + (kk%4) 32 B and K at +(kk/4) 8 KB + (kk%4) 32 B.
+// Key-tile halves.  Each CTA holds keys [64 rank, 64 rank + 64) of a 128-key
+// tile; half h of the tile is rows [32 h, 32 h + 32) of both CTAs' halves (the
+// pair MMA takes B's first 32 columns from the even CTA, the next 32 from the
+// odd one), so S column c of half h is key 32 h + c (c < 32) or
+// 64 + 32 h + (c - 32) (c >= 32) of the tile.  The half's 32 rows start
+// 32 x 128 B = 4 KB into each CTA's K half-tile (a whole number of 1 KB swizzle
+// atoms).
+constexpr uint32_t kHalfKeyRowsBytes = 32 * 128;
+
+// Key offset within the 128-key tile of S column c (0..63) of half h.
+__device__ __forceinline__ int half_key(int c, int h) { return 32 * h + c + (c >= 32 ? 32 : 0); }
+
+// S half (TMEM, 128 x 64 fp32 in each CTA) = Q (smem, K-major) * K^T (smem,
+// K-major, 32 keys per CTA): 8 pair MMAs of K = 16 in one block.  Step kk
+// reads Q at +(kk/4) 16 KB + (kk%4) 32 B and K at +(kk/4) 8 KB + (kk%4) 32 B.
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
   const uint32_t qa = desc_lo(q_smem, 16), kb = desc_lo(k_smem, 16);
   asm volatile(
-      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 a, b;\n\t.reg .b32 x, y;\n\t"
+      "{\n\t.reg .pred p0, p1, e;\n\telect.sync _|e, 0xffffffff;\n\t.reg .b64 a, b;\n\t.reg .b32 x, y;\n\t"
       "setp.ne.u32 p0, %4, %4;\n\t"
       "setp.eq.u32 p1, %4, %4;\n\t"
       "mov.b64 a, {%1, %3};\n\tmov.b64 b, {%2, %3};\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %5, p0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %5, p0;\n\t"
       "add.u32 x, %1, 2;\n\tadd.u32 y, %2, 2;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %5, p1;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %5, p1;\n\t"
       "add.u32 x, %1, 4;\n\tadd.u32 y, %2, 4;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %5, p1;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %5, p1;\n\t"
       "add.u32 x, %1, 6;\n\tadd.u32 y, %2, 6;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %5, p1;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %5, p1;\n\t"
       "add.u32 x, %1, 1024;\n\tadd.u32 y, %2, 512;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %5, p1;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %5, p1;\n\t"
       "add.u32 x, %1, 1026;\n\tadd.u32 y, %2, 514;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %5, p1;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %5, p1;\n\t"
       "add.u32 x, %1, 1028;\n\tadd.u32 y, %2, 516;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %5, p1;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %5, p1;\n\t"
       "add.u32 x, %1, 1030;\n\tadd.u32 y, %2, 518;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %5, p1;\n\t}" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], a, b, %5, p1;\n\t}" ::"r"(d_tmem),
       "r"(qa), "r"(kb), "r"(kDescHi), "r"(0u), "r"(kIdescQK)
       : "memory");
 }
 
-// O (TMEM fp32) (+)= P (TMEM, bf16 pairs) * V (smem, MN-major, 64 dims per CTA):
-// 8 pair MMAs of K = 16 keys in one block.  Step kk reads P at TMEM column
-// +8 kk and V at +2 KB kk; the first accumulates only if acc.
+// O (TMEM fp32) (+)= P (TMEM, bf16 pairs: 32 columns for the half's 64 keys)
+// * V (smem, MN-major, 64 dims per CTA), 4 pair MMAs of K = 16 keys.  MMA i
+// reads P columns +8 i, i.e. S columns [16 i, 16 i + 16) of the half, whose
+// keys are V's 16-key chunk 2h + {0, 1, 4, 5}[i] (2 KB apart in the slot):
+// v_smem is chunk 2h's address; the first MMA accumulates only if acc.
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, bool acc) {
   const uint32_t vb = desc_lo(v_smem, Cfg<false>::SlotBytes);
   asm volatile(
-      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 b;\n\t.reg .b32 t, y;\n\t"
+      "{\n\t.reg .pred p0, p1, e;\n\telect.sync _|e, 0xffffffff;\n\t.reg .b64 b;\n\t.reg .b32 t, y;\n\t"
       "setp.ne.u32 p0, %4, 0;\n\t"
       "setp.eq.u32 p1, %4, %4;\n\t"
       "mov.b64 b, {%2, %3};\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], b, %5, p0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], b, %5, p0;\n\t"
       "add.u32 t, %1, 8;\n\tadd.u32 y, %2, 128;\n\tmov.b64 b, {y, %3};\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], [t], b, %5, p1;\n\t"
-      "add.u32 t, %1, 16;\n\tadd.u32 y, %2, 256;\n\tmov.b64 b, {y, %3};\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], [t], b, %5, p1;\n\t"
-      "add.u32 t, %1, 24;\n\tadd.u32 y, %2, 384;\n\tmov.b64 b, {y, %3};\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], [t], b, %5, p1;\n\t"
-      "add.u32 t, %1, 32;\n\tadd.u32 y, %2, 512;\n\tmov.b64 b, {y, %3};\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], [t], b, %5, p1;\n\t"
-      "add.u32 t, %1, 40;\n\tadd.u32 y, %2, 640;\n\tmov.b64 b, {y, %3};\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], [t], b, %5, p1;\n\t"
-      "add.u32 t, %1, 48;\n\tadd.u32 y, %2, 768;\n\tmov.b64 b, {y, %3};\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], [t], b, %5, p1;\n\t"
-      "add.u32 t, %1, 56;\n\tadd.u32 y, %2, 896;\n\tmov.b64 b, {y, %3};\n\t"
-      "tcgen05.mma.cta_group::2.kind::f16 [%0], [t], b, %5, p1;\n\t}" ::"r"(d_tmem),
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [t], b, %5, p1;\n\t"
+      "add.u32 t, %1, 16;\n\tadd.u32 y, %2, 512;\n\tmov.b64 b, {y, %3};\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [t], b, %5, p1;\n\t"
+      "add.u32 t, %1, 24;\n\tadd.u32 y, %2, 640;\n\tmov.b64 b, {y, %3};\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f16 [%0], [t], b, %5, p1;\n\t}" ::"r"(d_tmem),
       "r"(p_tmem), "r"(vb), "r"(kDescHi), "r"(acc ? 1u : 0u), "r"(kIdescPV)
       : "memory");
 }
 
-// FP8: S = Q (e4m3, 128-byte rows) * K^T (e4m3, 64 keys per CTA), 4 pair MMAs
-// of K = 32 (32 bytes of each row per step).
+// FP8: S half = Q (e4m3, 128-byte rows) * K^T (e4m3, 32 keys per CTA), 4 pair
+// MMAs of K = 32 (32 bytes of each row per step).
 __device__ __forceinline__ void issue_qk_f8(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
   const uint32_t qa = desc_lo(q_smem, 16), kb = desc_lo(k_smem, 16);
   asm volatile(
-      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 a, b;\n\t.reg .b32 x, y;\n\t"
+      "{\n\t.reg .pred p0, p1, e;\n\telect.sync _|e, 0xffffffff;\n\t.reg .b64 a, b;\n\t.reg .b32 x, y;\n\t"
       "setp.ne.u32 p0, %4, %4;\n\t"
       "setp.eq.u32 p1, %4, %4;\n\t"
       "mov.b64 a, {%1, %3};\n\tmov.b64 b, {%2, %3};\n\t"
-      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], a, b, %5, p0;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], a, b, %5, p0;\n\t"
       "add.u32 x, %1, 2;\n\tadd.u32 y, %2, 2;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
-      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], a, b, %5, p1;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], a, b, %5, p1;\n\t"
       "add.u32 x, %1, 4;\n\tadd.u32 y, %2, 4;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
-      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], a, b, %5, p1;\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], a, b, %5, p1;\n\t"
       "add.u32 x, %1, 6;\n\tadd.u32 y, %2, 6;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
-      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], a, b, %5, p1;\n\t}" ::"r"(d_tmem),
-      "r"(qa), "r"(kb), "r"(kDescHi), "r"(0u), "r"(kIdescF8)
+      "@e tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], a, b, %5, p1;\n\t}" ::"r"(d_tmem),
+      "r"(qa), "r"(kb), "r"(kDescHi), "r"(0u), "r"(kIdescF8QK)
       : "memory");
 }
 
-// FP8: O (+)= P (TMEM, e4m3, four per column) * V (e4m3, K-major: 64 channels
-// per CTA, 128-byte rows of keys), 4 pair MMAs of K = 32 keys.
+// FP8: O (+)= P (TMEM, e4m3 four per column: 16 columns for the half's 64
+// keys) * V (e4m3, K-major: 64 channels per CTA, 128-byte rows of keys), 2
+// pair MMAs of K = 32 keys.  MMA i reads P columns +8 i, whose keys are the
+// 32-key chunk h + 2 i of V's rows (32 bytes apart): v_smem + 32 h is chunk h.
 __device__ __forceinline__ void issue_pv_f8(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, bool acc) {
   const uint32_t vb = desc_lo(v_smem, 16);
   asm volatile(
-      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 b;\n\t.reg .b32 t, y;\n\t"
+      "{\n\t.reg .pred p0, p1, e;\n\telect.sync _|e, 0xffffffff;\n\t.reg .b64 b;\n\t.reg .b32 t, y;\n\t"
       "setp.ne.u32 p0, %4, 0;\n\t"
       "setp.eq.u32 p1, %4, %4;\n\t"
       "mov.b64 b, {%2, %3};\n\t"
-      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], [%1], b, %5, p0;\n\t"
-      "add.u32 t, %1, 8;\n\tadd.u32 y, %2, 2;\n\tmov.b64 b, {y, %3};\n\t"
-      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], [t], b, %5, p1;\n\t"
-      "add.u32 t, %1, 16;\n\tadd.u32 y, %2, 4;\n\tmov.b64 b, {y, %3};\n\t"
-      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], [t], b, %5, p1;\n\t"
-      "add.u32 t, %1, 24;\n\tadd.u32 y, %2, 6;\n\tmov.b64 b, {y, %3};\n\t"
-      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], [t], b, %5, p1;\n\t}" ::"r"(d_tmem),
-      "r"(p_tmem), "r"(vb), "r"(kDescHi), "r"(acc ? 1u : 0u), "r"(kIdescF8)
+      "@e tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], [%1], b, %5, p0;\n\t"
+      "add.u32 t, %1, 8;\n\tadd.u32 y, %2, 4;\n\tmov.b64 b, {y, %3};\n\t"
+      "@e tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], [t], b, %5, p1;\n\t}" ::"r"(d_tmem),
+      "r"(p_tmem), "r"(vb), "r"(kDescHi), "r"(acc ? 1u : 0u), "r"(kIdescF8PV)
+      : "memory");
+}
+
+// The MMA warp runs its loop with all 32 lanes (warp-uniform values); each
+// tcgen05 instruction is issued by one elected lane.  Commit: arrive on the
+// barrier at this offset in both CTAs once the pair MMAs issued so far are done.
+__device__ __forceinline__ void commit_pair_elect(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n\t}" ::"r"(bar),
+      "h"(kPairMask)
+      : "memory");
+}
+__device__ __forceinline__ void commit_pair_local_elect(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
       : "memory");
 }
 
@@ -293,16 +340,17 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   return r;
 }
 
-// One query row's 128 scores from TMEM (4 loads of 32 columns); keys past
-// the document end (column >= rem) are set to -inf.
-__device__ __forceinline__ void load_scores(uint32_t t_s, uint32_t (&r)[4][32], int rem) {
-#pragma unroll
-  for (int c = 0; c < 4; ++c) dev::tmem_ld32(t_s + c * 32, r[c]);
+// One query row's 64 scores of key-tile half h from TMEM (2 loads of 32
+// columns); keys past the document end (key offset within the tile >= rem)
+// are set to -inf.
+__device__ __forceinline__ void load_scores(uint32_t t_s, uint32_t (&r)[2][32], int rem, int h) {
+  dev::tmem_ld32(t_s, r[0]);
+  dev::tmem_ld32(t_s + 32, r[1]);
   dev::tmem_wait_ld();
   if (rem < kTileRows) {
 #pragma unroll
-    for (int c = 0; c < 128; ++c)
-      if (c >= rem) r[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+    for (int c = 0; c < 64; ++c)
+      if (half_key(c, h) >= rem) r[c >> 5][c & 31] = __float_as_uint(-INFINITY);
   }
 }
 
@@ -424,9 +472,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       dev::mbar_init(bars.q_ready(i), 2);           // the Q warp of each CTA of the pair
     }
     for (int s = 0; s < 2; ++s) {
-      dev::mbar_init(bars.s_ready(s), 1);
-      dev::mbar_init(bars.p_ready(s), 8);           // one arrival per softmax warp of the pair
-      dev::mbar_init(bars.o_ready(s), 1);
+      for (int h = 0; h < 2; ++h) {
+        dev::mbar_init(bars.s_ready(s, h), 1);
+        dev::mbar_init(bars.p_ready(s, h), 8);      // one arrival per softmax warp of the pair
+        dev::mbar_init(bars.pv_done(s, h), 1);
+      }
     }
     for (int i = 0; i < kGroups; ++i) {
       dev::mbar_init(bars.kv_full(i), 1);
@@ -531,140 +581,135 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ----------------------------------------- MMA issuer (even CTA, pair) ----
-    if (lane == 0 && rank == 0) {
+    // The whole warp runs the loop (its values stay warp-uniform); every
+    // tcgen05 MMA and commit is issued by one elected lane.
+    if (rank == 0) {
       // ring slots of the current group's V and K halves: group n uses slots
       // 2n-1 and 2n (mod kSlots), advanced by two per key tile without a division
-      uint32_t vslot = 1, kslot = 2, q_use[4] = {0, 0, 0, 0}, p_it0 = 0, p_it1 = 0;
+      uint32_t vslot = 1, kslot = 2, q_use[4] = {0, 0, 0, 0};
+      uint32_t p_it[2][2] = {{0, 0}, {0, 0}};
       bool ok = true;
       bool issued = false;
       int k = 0;
-      if constexpr (kFp8) {
-        for (int u = u_begin; ok && u < u_end; ++u, ++k) {
-          const UnitGeom g = unit_geom(a.units, u);
-          const uint32_t qb = 2 * (k & 1);
-          // Q tiles of this unit, prepared in both CTAs (and, for the first
-          // unit, the first K group landed in both)
-#pragma unroll
-          for (int s = 0; s < 2; ++s) {
-            if (!ok || s >= g.n_st) break;
-            ok = dev::mbar_wait(bars.q_ready(qb + s), q_use[qb + s] & 1, abort_flag, a.err, kTimeoutNs);
-            ++q_use[qb + s];
-          }
-          // this unit's first K tile: group 0, or the K half of the previous
-          // unit's last group (covered by that unit's last P-ready barrier)
-          const uint32_t k0 = k == 0 ? 0u : (kslot >= 2 ? kslot - 2 : kslot + kSlots - 2);
-          if (!ok) break;
-          dev::tc_fence_after();
-#pragma unroll
-          for (int s = 0; s < 2; ++s) {
-            if (s >= g.n_st) break;
-            issue_qk_f8(tmem + s * 128, sbase + C::SmemQ + (qb + s) * C::QTileBytes,
-                        sbase + C::SmemKV + k0 * C::SlotBytes);
-            dev::mma_commit_pair_mc(bars.s_ready(s), kPairMask);
-            if (g.hi - g.lo == 1) dev::mma_commit_pair_mc(bars.q_empty(qb + s), kPairMask);
-          }
-          issued = true;
-          for (int j = g.lo; j < g.hi; ++j) {
-            // group grp = V(j) + the next K tile; its arrival in both CTAs is
-            // implied by P-ready of query tile 0
-            const bool more = j + 1 < g.hi;
-#pragma unroll
-            for (int s = 0; s < 2; ++s) {
-              if (s >= g.n_st) break;
-              uint32_t& p_it = s == 0 ? p_it0 : p_it1;
-              ok = dev::mbar_wait(bars.p_ready(s), p_it & 1, abort_flag, a.err, kTimeoutNs);
-              if (!ok) break;
-              ++p_it;
-              dev::tc_fence_after();
-              issue_pv_f8(tmem + 256 + s * 128, tmem + s * 128, sbase + C::SmemKV + vslot * C::SlotBytes, j > g.lo);
-              if (more) {
-                issue_qk_f8(tmem + s * 128, sbase + C::SmemQ + (qb + s) * C::QTileBytes,
-                            sbase + C::SmemKV + kslot * C::SlotBytes);
-                dev::mma_commit_pair_mc(bars.s_ready(s), kPairMask);
-                if (j + 2 == g.hi) dev::mma_commit_pair_mc(bars.q_empty(qb + s), kPairMask);
-              } else {
-                dev::mma_commit_pair_mc(bars.o_ready(s), kPairMask);
-              }
-            }
-            if (!ok) break;
-            vslot = vslot + 2 >= (uint32_t)kSlots ? vslot + 2 - kSlots : vslot + 2;
-            kslot = kslot + 2 >= (uint32_t)kSlots ? kslot + 2 - kSlots : kslot + 2;
-          }
-        }
-      } else {
-        // bf16: a unit's first QKs are issued during the last key tile of the
-        // unit before, so the tensor pipe has them queued while the softmax
-        // warps write that unit's output.
-        // The first QK of query tile s of unit gg: Q slot qbase + s (once the
-        // tile is prepared in both CTAs), K in ring slot ks.
-        auto first_qk = [&](const UnitGeom& gg, uint32_t qbase, uint32_t ks, int s) {
-          ok = dev::mbar_wait(bars.q_ready(qbase + s), q_use[qbase + s] & 1, abort_flag, a.err, kTimeoutNs);
+      // QK of half h of the key tile in ring slot ks for query tile s (Q slot qs)
+      auto qk_half = [&](int s, uint32_t qs, uint32_t ks, int h) {
+        const uint32_t d = tmem + s * 128 + h * 64;
+        const uint32_t qa = sbase + C::SmemQ + qs * C::QTileBytes;
+        const uint32_t kb = sbase + C::SmemKV + ks * C::SlotBytes + h * kHalfKeyRowsBytes;
+        if constexpr (kFp8)
+          issue_qk_f8(d, qa, kb);
+        else
+          issue_qk(d, qa, kb);
+        commit_pair_elect(bars.s_ready(s, h));
+      };
+      // PV of half h of the key tile whose V is in ring slot vs, query tile s
+      auto pv_half = [&](int s, uint32_t vs, int h, bool acc) {
+        const uint32_t d = tmem + 256 + s * 128, pt = tmem + s * 128 + h * 64;
+        const uint32_t vb = sbase + C::SmemKV + vs * C::SlotBytes;
+        if constexpr (kFp8)
+          issue_pv_f8(d, pt, vb + 32 * h, acc);
+        else
+          issue_pv(d, pt, vb + 4096 * h, acc);
+      };
+      // The first QK (half h) of query tile s of unit gg: Q slot qbase + s (its
+      // readiness in both CTAs is awaited before half 0), K in ring slot ks.
+      auto first_qk = [&](const UnitGeom& gg, uint32_t qbase, uint32_t ks, int s, int h) {
+        if (h == 0) {
+          ok = __all_sync(0xffffffffu,
+                          dev::mbar_wait(bars.q_ready(qbase + s), q_use[qbase + s] & 1, abort_flag, a.err, kTimeoutNs));
           ++q_use[qbase + s];
           if (!ok) return;
           dev::tc_fence_after();
-          issue_qk(tmem + s * 128, sbase + C::SmemQ + (qbase + s) * C::QTileBytes, sbase + C::SmemKV + ks * C::SlotBytes);
-          dev::mma_commit_pair_mc(bars.s_ready(s), kPairMask);
-          if (gg.hi - gg.lo == 1) dev::mma_commit_pair_mc(bars.q_empty(qbase + s), kPairMask);
-          issued = true;
-        };
-        for (int u = u_begin; ok && u < u_end; ++u, ++k) {
-          const UnitGeom g = unit_geom(a.units, u);
-          const uint32_t qb = 2 * (k & 1);
-          if (k == 0) {
-            // the pair's first unit: its first K tile is group 0 (ring slot
-            // 0), and Q-ready also covers that group's arrival in both CTAs
-            for (int s = 0; ok && s < g.n_st; ++s) first_qk(g, qb, 0, s);
-            if (!ok) break;
-          }
-          // The next unit's first K tile is the K half of this unit's last
-          // group (ring slot kslot in the last key tile).  Its QK of query
-          // tile s goes right after this unit's PV of tile s when the next
-          // unit has at least as many query tiles (then the MMAs that the ring
-          // release of its first key tile waits for include every PV of this
-          // unit); otherwise after both PVs.
-          const bool has_next = u + 1 < u_end;
-          const UnitGeom gn = unit_geom(a.units, has_next ? u + 1 : u);
-          const uint32_t qn = 2 * ((k + 1) & 1);
-          const bool early = has_next && gn.n_st >= g.n_st;
-          for (int j = g.lo; j < g.hi; ++j) {
-            // group grp = V(j) + the next K tile; its arrival in both CTAs is
-            // implied by P-ready of query tile 0
-            const bool more = j + 1 < g.hi;
+        }
+        qk_half(s, qbase + s, ks, h);
+        if (h == 1 && gg.hi - gg.lo == 1) commit_pair_elect(bars.q_empty(qbase + s));
+        issued = true;
+      };
+      for (int u = u_begin; ok && u < u_end; ++u, ++k) {
+        const UnitGeom g = unit_geom(a.units, u);
+        const uint32_t qb = 2 * (k & 1);
+        if (k == 0) {
+          // the pair's first unit: its first K tile is group 0 (ring slot 0),
+          // and Q-ready also covers that group's arrival in both CTAs
+          for (int h = 0; ok && h < 2; ++h)
+            for (int s = 0; ok && s < g.n_st; ++s) first_qk(g, qb, 0, s, h);
+          if (!ok) break;
+        }
+        // Per key tile j and half h, for each query tile s: wait for P(s, j, h),
+        // then PV(s, j, h) and QK(s, j + 1, h) -- the next key tile's S half
+        // goes where P(s, j, h) was, and the softmax works on the other half
+        // meanwhile.  In the last key tile the next unit's first QKs take the
+        // place of QK(s, j + 1, h).  The next unit's first key tile is the K
+        // half of this unit's last group (ring slot kslot in the last key
+        // tile); its group is released when the next unit's last query tile
+        // sees S of half 1, so that QK is issued after every PV of this unit
+        // (held back to the end when the next unit has fewer query tiles).
+        const bool has_next = u + 1 < u_end;
+        const UnitGeom gn = unit_geom(a.units, has_next ? u + 1 : u);
+        const uint32_t qn = 2 * ((k + 1) & 1);
+        const bool fewer_next = has_next && gn.n_st < g.n_st;
+        const bool two = g.n_st == 2;
+        // steady state: key tiles with a next key tile in this unit
+        for (int j = g.lo; ok && j + 1 < g.hi; ++j) {
+          const bool acc0 = j > g.lo;
+          const bool last_qk = j + 2 == g.hi;  // QK(., j + 1, 1) is the unit's last QK of the tile
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
 #pragma unroll
             for (int s = 0; s < 2; ++s) {
-              if (s >= g.n_st) break;
-              uint32_t& p_it = s == 0 ? p_it0 : p_it1;
-              ok = dev::mbar_wait(bars.p_ready(s), p_it & 1, abort_flag, a.err, kTimeoutNs);
+              if (s == 1 && !two) break;
+              // one lane polls P; the warp follows it
+              bool good = true;
+              if (lane == 0) good = dev::mbar_wait(bars.p_ready(s, h), p_it[s][h] & 1, abort_flag, a.err, kTimeoutNs);
+              ok = __shfl_sync(0xffffffffu, good, 0);
               if (!ok) break;
-              ++p_it;
+              ++p_it[s][h];
               dev::tc_fence_after();
-              issue_pv(tmem + 256 + s * 128, tmem + s * 128, sbase + C::SmemKV + vslot * C::SlotBytes, j > g.lo);
-              if (more) {
-                issue_qk(tmem + s * 128, sbase + C::SmemQ + (qb + s) * C::QTileBytes,
-                         sbase + C::SmemKV + kslot * C::SlotBytes);
-                dev::mma_commit_pair_mc(bars.s_ready(s), kPairMask);
-                if (j + 2 == g.hi) dev::mma_commit_pair_mc(bars.q_empty(qb + s), kPairMask);
-              } else {
-                dev::mma_commit_pair_mc(bars.o_ready(s), kPairMask);
-                if (early) {
-                  first_qk(gn, qn, kslot, s);
-                  if (!ok) break;
-                }
+              pv_half(s, vslot, h, acc0 || h == 1);
+              qk_half(s, qb + s, kslot, h);
+              if (h == 1 && last_qk) commit_pair_elect(bars.q_empty(qb + s));
+            }
+            if (!ok) break;
+          }
+          vslot = vslot + 2 >= (uint32_t)kSlots ? vslot + 2 - kSlots : vslot + 2;
+          kslot = kslot + 2 >= (uint32_t)kSlots ? kslot + 2 - kSlots : kslot + 2;
+        }
+        if (!ok) break;
+        // the last key tile: each PV is followed by "PV done" of its half (the
+        // epilogue waits for it), and the next unit's first QKs take the place
+        // of QK(s, j + 1, h); the QK that releases the next unit's first K/V
+        // group in the ring comes after every PV of this unit
+        {
+          const bool acc0 = g.hi - 1 > g.lo;
+          for (int h = 0; ok && h < 2; ++h) {
+#pragma unroll 1
+            for (int s = 0; s < g.n_st; ++s) {
+              ok = __all_sync(0xffffffffu,
+                              dev::mbar_wait(bars.p_ready(s, h), p_it[s][h] & 1, abort_flag, a.err, kTimeoutNs));
+              if (!ok) break;
+              ++p_it[s][h];
+              dev::tc_fence_after();
+              pv_half(s, vslot, h, acc0 || h == 1);
+              commit_pair_elect(bars.pv_done(s, h));
+              if (has_next && s < gn.n_st && !(h == 1 && fewer_next && s == gn.n_st - 1)) {
+                first_qk(gn, qn, kslot, s, h);
+                if (!ok) break;
               }
             }
             if (!ok) break;
-            if (!more && has_next) {
-              for (int s = early ? g.n_st : 0; ok && s < gn.n_st; ++s) first_qk(gn, qn, kslot, s);
-              if (!ok) break;
+            if (has_next) {
+              for (int s = 0; ok && s < gn.n_st; ++s)
+                if (s >= g.n_st || (h == 1 && fewer_next && s == gn.n_st - 1)) first_qk(gn, qn, kslot, s, h);
             }
-            vslot = vslot + 2 >= (uint32_t)kSlots ? vslot + 2 - kSlots : vslot + 2;
-            kslot = kslot + 2 >= (uint32_t)kSlots ? kslot + 2 - kSlots : kslot + 2;
           }
+          vslot = vslot + 2 >= (uint32_t)kSlots ? vslot + 2 - kSlots : vslot + 2;
+          kslot = kslot + 2 >= (uint32_t)kSlots ? kslot + 2 - kSlots : kslot + 2;
         }
       }
       if (!ok && issued) {
         // drain: every MMA issued so far must finish before TMEM is freed
-        dev::mma_commit_pair(bars.drain());
+        __syncwarp();
+        commit_pair_local_elect(bars.drain());
         dev::mbar_wait_bounded(bars.drain(), 0, nullptr, nullptr, kTimeoutNs);
       }
     }
@@ -711,9 +756,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = (warp & 3) * 32;
     const uint32_t t_s = tmem + (lane_base << 16) + st * 128;        // S_s / P_s
     const uint32_t t_o = tmem + (lane_base << 16) + 256 + st * 128;  // O_s
-    const uint32_t p_ready_remote = dev::mapa_shared(bars.p_ready(st), 0);
+    const uint32_t p_ready_remote[2] = {dev::mapa_shared(bars.p_ready(st, 0), 0),
+                                        dev::mapa_shared(bars.p_ready(st, 1), 0)};
     const bool lead_lane = (warp & 3) == 0 && lane == 0;             // one lane per warpgroup
-    uint32_t s_it = 0, o_it = 0;
+    uint32_t s_it[2] = {0, 0};
+    uint32_t n_done = 0;                 // units this query tile has finished (PV-done phases per half)
     uint32_t t0 = 0;                     // key tiles the pair has started before this unit
     bool ok = true;
     const float sl2 = a.scale_log2;
@@ -735,62 +782,66 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int32_t row = g.q0 + st * 2 * kTileRows + (int32_t)rank * kTileRows + (int32_t)row_in_tile;
         if (row < a.S) sq_row = __ldg(a.sq + (int64_t)g.head * a.S + row);
       }
-      for (int j = g.lo; j < g.hi; ++j) {
+      for (int j = g.lo; ok && j < g.hi; ++j) {
         const uint32_t t = t_unit + (j - g.lo);  // the pair's running key-tile count
         // score scale in log2 units: softmax_scale log2(e), times the q-row and
         // key-tile scales for fp8
         float rsc = sl2;
         if constexpr (kFp8) rsc = sl2 * sq_row * __ldg(a.sk + (int64_t)g.head * a.S + g.kv0 + j * kTileRows);
-        ok = dev::mbar_wait(bars.s_ready(st), s_it & 1, abort_flag, a.err, kTimeoutNs);
-        if (!ok) break;
-        ++s_it;
-        // S of the last query tile is ready: every MMA before it is done, so
-        // the group holding K(t) (and V(t-1)) is free in this CTA
-        if (releases) dev::mbar_arrive(bars.kv_empty(t % kGroups));
-        // fp8 (whose per-tile softmax loop sets the period): test, without
-        // blocking, whether the next K/V group has landed; the blocking wait
-        // below then only runs if it had not
-        uint32_t kv_bar = 0, kv_par = 0;
-        bool kv_landed = false;
-        if constexpr (kFp8) {
-          kv_bar = bars.kv_full((t + 1) % kGroups);
-          kv_par = ((t + 1) / kGroups) & 1;
-          kv_landed = checks_kv && dev::mbar_test_wait(kv_bar, kv_par);
-        }
-        __syncwarp();  // lanes leave the wait separately; the TMEM loads are warp-collective
-        dev::tc_fence_after();
-        uint32_t r[4][32];
-        float* sv = reinterpret_cast<float*>(&r[0][0]);
         const int rem = g.kv1 - (g.kv0 + j * kTileRows);
-        load_scores(t_s, r, rem);
-        // Row max: eight independent chains of 3-input maxima.
-        float mx[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) mx[i] = fmaxf(sv[i], sv[8 + i]);
-#pragma unroll
-        for (int c = 16; c < 128; c += 16)
-#pragma unroll
-          for (int i = 0; i < 8; ++i) mx[i] = dev::max3(mx[i], sv[c + i], sv[c + 8 + i]);
-        const float m_new =
-            dev::max3(dev::max3(mx[0], mx[1], mx[2]), dev::max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * rsc;
-        // The reference max only moves when the row max grows by more than
-        // 2^8 (then O and l are rescaled; the final O / l is unchanged).  The
-        // O row is rescaled after P is written: the next PV waits for p_ready.
-        float alpha = 1.f;
-        if (m_new > m_used + kRescaleThreshold) {
-          alpha = dev::ex2_approx(m_used - m_new);  // 0 on the first tile (m_used = -inf)
-          m_used = m_new;
-        }
-        const float neg = -m_used;
-        float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        // fp8: test, without blocking, whether the next K/V group has landed;
+        // the blocking wait before half 0's P is reported then only runs if
+        // not (bf16 measured faster with the plain blocking wait)
+        const uint32_t kv_bar = bars.kv_full((t + 1) % kGroups), kv_par = ((t + 1) / kGroups) & 1;
+        const bool kv_landed = kFp8 && checks_kv && dev::mbar_test_wait(kv_bar, kv_par);
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
+          ok = dev::mbar_wait(bars.s_ready(st, h), s_it[h] & 1, abort_flag, a.err, kTimeoutNs);
+          if (!ok) break;
+          ++s_it[h];
+          // S half 1 of the last query tile is ready: every MMA before its QK is
+          // done, so the group holding K(t) (and V(t-1)) is free in this CTA
+          if (releases && h == 1) dev::mbar_arrive(bars.kv_empty(t % kGroups));
+          __syncwarp();  // lanes leave the wait separately; the TMEM loads are warp-collective
+          dev::tc_fence_after();
+          const uint32_t t_sh = t_s + 64 * h;  // this half's S, then its P
+          uint32_t r[2][32];
+          dev::tmem_ld32(t_sh, r[0]);
+          dev::tmem_ld32(t_sh + 32, r[1]);
+          dev::tmem_wait_ld();
+          float sv[64];
+#pragma unroll
+          for (int c = 0; c < 64; ++c) sv[c] = __uint_as_float(r[c >> 5][c & 31]);
+          if (rem < kTileRows) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c)
+              if (half_key(c, h) >= rem) sv[c] = -INFINITY;
+          }
+          // Row max of the half: eight independent chains of 3-input maxima.
+          float mx[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) mx[i] = fmaxf(sv[i], sv[8 + i]);
+#pragma unroll
+          for (int c = 16; c < 64; c += 16)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx[i] = dev::max3(mx[i], sv[c + i], sv[c + 8 + i]);
+          const float m_new =
+              dev::max3(dev::max3(mx[0], mx[1], mx[2]), dev::max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * rsc;
+          // The reference max only moves when the row max grows by more than
+          // 2^8 (then O and l are rescaled; the final O / l is unchanged).
+          float alpha = 1.f;
+          if (m_new > m_used + kRescaleThreshold) {
+            alpha = dev::ex2_approx(m_used - m_new);  // 0 on the first half of a unit (m_used = -inf)
+            m_used = m_new;
+          }
+          const float neg = -m_used;
+          float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
           uint32_t p[32];
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             // packed pair arithmetic: one f32x2 FMA for the exponents, one f32x2 add for the sums
             float x0, x1;
-            dev::fma2(x0, x1, sv[64 * h + 2 * c], sv[64 * h + 2 * c + 1], rsc, rsc, neg, neg);
+            dev::fma2(x0, x1, sv[2 * c], sv[2 * c + 1], rsc, rsc, neg, neg);
             const float p0 = dev::ex2_approx(x0), p1 = dev::ex2_approx(x1);
             const int ai = 2 * (c & 3);
             dev::add2(rs8[ai], rs8[ai + 1], rs8[ai], rs8[ai + 1], p0, p1);
@@ -806,52 +857,63 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t p16[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) p16[i] = p[i];
-            dev::tmem_st16(t_s + 16 * h, p16);
+            dev::tmem_st16(t_sh, p16);
           } else {
-            dev::tmem_st32(t_s + 32 * h, p);
+            dev::tmem_st32(t_sh, p);
           }
-        }
-        const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
-        l = l * alpha + rs;
-        // tcgen05.ld/st are warp-collective (.sync.aligned): the rescale runs
-        // for the whole warp when any of its rows needs it (alpha = 1 elsewhere).
-        if (j > g.lo && __any_sync(0xffffffffu, alpha != 1.f)) {
+          const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+          l = l * alpha + rs;
+          // tcgen05.ld/st are warp-collective (.sync.aligned): the rescale runs
+          // for the whole warp when any of its rows needs it (alpha = 1
+          // elsewhere).  The PV of the previous half (the other half) may
+          // still be adding into O (every earlier PV of this tile completed
+          // before the QK whose S was just read), so it is awaited first: the
+          // QK issued right after it fills the other half's next S, which this
+          // thread reads next anyway; in the last key tile no such QK may
+          // follow, and "PV done" of half 0 is awaited instead.
+          if (!(j == g.lo && h == 0) && __any_sync(0xffffffffu, alpha != 1.f)) {
+            if (h == 1 && j + 1 == g.hi)
+              ok = dev::mbar_wait(bars.pv_done(st, 0), n_done & 1, abort_flag, a.err, kTimeoutNs);
+            else
+              ok = dev::mbar_wait(bars.s_ready(st, 1 - h), s_it[1 - h] & 1, abort_flag, a.err, kTimeoutNs);
+            __syncwarp();
+            dev::tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < 8; ++c) {
+              uint32_t ov[16];
+              dev::tmem_ld16(t_o + c * 16, ov);
+              dev::tmem_wait_ld();
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            uint32_t ov[32];
-            dev::tmem_ld32(t_o + c * 32, ov);
-            dev::tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-            dev::tmem_st32(t_o + c * 32, ov);
+              for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+              dev::tmem_st16(t_o + c * 16, ov);
+            }
           }
-        }
-        dev::tmem_wait_st();
-        dev::tc_fence_before();
-        __syncwarp();
-        // the next PV reads V(t) and the QK after it K(t+1): group t+1 must have
-        // landed in this CTA before query tile 0 reports P ready
-        if constexpr (kFp8) {
-          if (checks_kv && !kv_landed) ok = dev::mbar_wait(kv_bar, kv_par, abort_flag, a.err, kTimeoutNs);
-        } else if (checks_kv) {
-          ok = dev::mbar_wait(bars.kv_full((t + 1) % kGroups), ((t + 1) / kGroups) & 1, abort_flag, a.err,
-                              kTimeoutNs);
-        }
-        if (lane == 0) {  // P (and O) of the warp's 32 rows
-          if (kFp8 && rank == 0)
-            dev::mbar_arrive(bars.p_ready(st));  // the even CTA's own barrier, arrived on locally
-          else
-            dev::mbar_arrive_cluster(p_ready_remote);
-        }
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
+          dev::tmem_wait_st();
+          dev::tc_fence_before();
+          __syncwarp();
+          // half 0's PV reads V(t) and the QK after it K(t+1): group t+1 must have
+          // landed in this CTA before query tile 0 reports that P ready
+          if (h == 0 && checks_kv && (kFp8 ? !kv_landed : true))
+            ok = dev::mbar_wait(kv_bar, kv_par, abort_flag, a.err, kTimeoutNs) && ok;
+          if (lane == 0) {  // P (and O) of the warp's 32 rows
+            if (kFp8 && rank == 0)  // fp8: the even CTA's own barrier, arrived on locally
+              dev::mbar_arrive(bars.p_ready(st, h));
+            else
+              dev::mbar_arrive_cluster(p_ready_remote[h]);
+          }
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
         }
       }
       if (!ok) break;
-      ok = dev::mbar_wait(bars.o_ready(st), o_it & 1, abort_flag, a.err, kTimeoutNs);
+      // the unit's last PVs of this query tile, one per half ("PV done" of a
+      // half completes once per unit, after its last key tile's PV)
+      ok = dev::mbar_wait(bars.pv_done(st, 0), n_done & 1, abort_flag, a.err, kTimeoutNs) &&
+           dev::mbar_wait(bars.pv_done(st, 1), n_done & 1, abort_flag, a.err, kTimeoutNs);
+      ++n_done;
       if (!ok) break;
-      ++o_it;
       __syncwarp();
       dev::tc_fence_after();
       const int32_t local = st * 2 * kTileRows + (int32_t)rank * kTileRows + (int32_t)row_in_tile;
