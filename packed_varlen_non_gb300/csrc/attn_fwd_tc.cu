@@ -80,9 +80,12 @@
 // on e4m3 Q, K and transposed V (channel rows of keys, every document
 // starting on a 16-key boundary) with fp32 scales -- kind::f8f6f4 pair MMAs of
 // K = 32, 16 KB Q tiles and 8 KB half-tiles in 128-byte rows, P rounded to
-// e4m3 and stored four per TMEM column (first 16 columns of an S half), the
-// q-row x key-tile scale folded into the softmax's score multiplier, the
-// per-channel V scale applied to O in the epilogue.
+// e4m3 and stored four per TMEM column (first 32 columns of S), the q-row x
+// key-tile scale folded into the softmax's score multiplier, the per-channel
+// V scale applied to O in the epilogue.  Its MMAs are half as long as bf16's,
+// so it keeps whole 128-key tiles (one S-ready and one P-ready phase per key
+// tile and query tile, P over S, issued by one thread): split into halves,
+// the per-half softmax costs measured slower than the chain they remove.
 //
 // Every mbarrier wait is bounded: on expiry the CTA raises an abort flag,
 // records a timeout in the device error word, drains its own copies and MMAs
@@ -138,10 +141,9 @@ static_assert(kUnitRows == 4 * kTileRows, "a unit is two query tiles in each CTA
 constexpr uint32_t kIdescBf16 = (1u << 4) | (1u << 7) | (1u << 10) | ((256u >> 4) << 24);
 constexpr uint32_t kIdescQK = kIdescBf16 | ((64u >> 3) << 17);
 constexpr uint32_t kIdescPV = kIdescBf16 | ((128u >> 3) << 17) | (1u << 16);
-// kind::f8f6f4: e4m3 A and B (type code 0), fp32 accumulator, M = 256, both
-// K-major; QK N = 64 keys, PV N = 128 dims
-constexpr uint32_t kIdescF8QK = (1u << 4) | ((64u >> 3) << 17) | ((256u >> 4) << 24);
-constexpr uint32_t kIdescF8PV = (1u << 4) | ((128u >> 3) << 17) | ((256u >> 4) << 24);
+// kind::f8f6f4: e4m3 A and B (type code 0), fp32 accumulator, M = 256, N = 128,
+// both K-major (the FP8 pipeline takes whole 128-key tiles)
+constexpr uint32_t kIdescF8 = (1u << 4) | ((128u >> 3) << 17) | ((256u >> 4) << 24);
 
 // Q slot i = 2 * buffer + query tile; the unit with ordinal k (per pair) uses buffer k & 1.
 struct Bars {
@@ -278,41 +280,44 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
       : "memory");
 }
 
-// FP8: S half = Q (e4m3, 128-byte rows) * K^T (e4m3, 32 keys per CTA), 4 pair
-// MMAs of K = 32 (32 bytes of each row per step).
+// FP8 (whole 128-key tiles, issued by one thread): S = Q (e4m3, 128-byte rows)
+// * K^T (e4m3, 64 keys per CTA), 4 pair MMAs of K = 32 (32 bytes of each row
+// per step).
 __device__ __forceinline__ void issue_qk_f8(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
   const uint32_t qa = desc_lo(q_smem, 16), kb = desc_lo(k_smem, 16);
   asm volatile(
-      "{\n\t.reg .pred p0, p1, e;\n\telect.sync _|e, 0xffffffff;\n\t.reg .b64 a, b;\n\t.reg .b32 x, y;\n\t"
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 a, b;\n\t.reg .b32 x, y;\n\t"
       "setp.ne.u32 p0, %4, %4;\n\t"
       "setp.eq.u32 p1, %4, %4;\n\t"
       "mov.b64 a, {%1, %3};\n\tmov.b64 b, {%2, %3};\n\t"
-      "@e tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], a, b, %5, p0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], a, b, %5, p0;\n\t"
       "add.u32 x, %1, 2;\n\tadd.u32 y, %2, 2;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
-      "@e tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], a, b, %5, p1;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], a, b, %5, p1;\n\t"
       "add.u32 x, %1, 4;\n\tadd.u32 y, %2, 4;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
-      "@e tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], a, b, %5, p1;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], a, b, %5, p1;\n\t"
       "add.u32 x, %1, 6;\n\tadd.u32 y, %2, 6;\n\tmov.b64 a, {x, %3};\n\tmov.b64 b, {y, %3};\n\t"
-      "@e tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], a, b, %5, p1;\n\t}" ::"r"(d_tmem),
-      "r"(qa), "r"(kb), "r"(kDescHi), "r"(0u), "r"(kIdescF8QK)
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], a, b, %5, p1;\n\t}" ::"r"(d_tmem),
+      "r"(qa), "r"(kb), "r"(kDescHi), "r"(0u), "r"(kIdescF8)
       : "memory");
 }
 
-// FP8: O (+)= P (TMEM, e4m3 four per column: 16 columns for the half's 64
-// keys) * V (e4m3, K-major: 64 channels per CTA, 128-byte rows of keys), 2
-// pair MMAs of K = 32 keys.  MMA i reads P columns +8 i, whose keys are the
-// 32-key chunk h + 2 i of V's rows (32 bytes apart): v_smem + 32 h is chunk h.
+// FP8: O (+)= P (TMEM, e4m3, four per column) * V (e4m3, K-major: 64 channels
+// per CTA, 128-byte rows of keys), 4 pair MMAs of K = 32 keys.
 __device__ __forceinline__ void issue_pv_f8(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem, bool acc) {
   const uint32_t vb = desc_lo(v_smem, 16);
   asm volatile(
-      "{\n\t.reg .pred p0, p1, e;\n\telect.sync _|e, 0xffffffff;\n\t.reg .b64 b;\n\t.reg .b32 t, y;\n\t"
+      "{\n\t.reg .pred p0, p1;\n\t.reg .b64 b;\n\t.reg .b32 t, y;\n\t"
       "setp.ne.u32 p0, %4, 0;\n\t"
       "setp.eq.u32 p1, %4, %4;\n\t"
       "mov.b64 b, {%2, %3};\n\t"
-      "@e tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], [%1], b, %5, p0;\n\t"
-      "add.u32 t, %1, 8;\n\tadd.u32 y, %2, 4;\n\tmov.b64 b, {y, %3};\n\t"
-      "@e tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], [t], b, %5, p1;\n\t}" ::"r"(d_tmem),
-      "r"(p_tmem), "r"(vb), "r"(kDescHi), "r"(acc ? 1u : 0u), "r"(kIdescF8PV)
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], [%1], b, %5, p0;\n\t"
+      "add.u32 t, %1, 8;\n\tadd.u32 y, %2, 2;\n\tmov.b64 b, {y, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], [t], b, %5, p1;\n\t"
+      "add.u32 t, %1, 16;\n\tadd.u32 y, %2, 4;\n\tmov.b64 b, {y, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], [t], b, %5, p1;\n\t"
+      "add.u32 t, %1, 24;\n\tadd.u32 y, %2, 6;\n\tmov.b64 b, {y, %3};\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], [t], b, %5, p1;\n\t}" ::"r"(d_tmem),
+      "r"(p_tmem), "r"(vb), "r"(kDescHi), "r"(acc ? 1u : 0u), "r"(kIdescF8)
       : "memory");
 }
 
@@ -340,17 +345,16 @@ __device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
   return r;
 }
 
-// One query row's 64 scores of key-tile half h from TMEM (2 loads of 32
-// columns); keys past the document end (key offset within the tile >= rem)
-// are set to -inf.
-__device__ __forceinline__ void load_scores(uint32_t t_s, uint32_t (&r)[2][32], int rem, int h) {
-  dev::tmem_ld32(t_s, r[0]);
-  dev::tmem_ld32(t_s + 32, r[1]);
+// FP8: one query row's 128 scores from TMEM (4 loads of 32 columns); keys past
+// the document end (column >= rem) are set to -inf.
+__device__ __forceinline__ void load_scores128(uint32_t t_s, uint32_t (&r)[4][32], int rem) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) dev::tmem_ld32(t_s + c * 32, r[c]);
   dev::tmem_wait_ld();
   if (rem < kTileRows) {
 #pragma unroll
-    for (int c = 0; c < 64; ++c)
-      if (half_key(c, h) >= rem) r[c >> 5][c & 31] = __float_as_uint(-INFINITY);
+    for (int c = 0; c < 128; ++c)
+      if (c >= rem) r[c >> 5][c & 31] = __float_as_uint(-INFINITY);
   }
 }
 
@@ -581,9 +585,75 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ----------------------------------------- MMA issuer (even CTA, pair) ----
-    // The whole warp runs the loop (its values stay warp-uniform); every
+    if constexpr (kFp8) {
+      // FP8: whole 128-key tiles (S of a query tile is one barrier phase, P
+      // overwrites it), issued by one thread.  Its MMAs are half as long as
+      // bf16's, and the halved pipeline measured slower here: the per-half
+      // softmax costs would dominate.
+      if (lane == 0 && rank == 0) {
+        uint32_t vslot = 1, kslot = 2, q_use[4] = {0, 0, 0, 0}, p_it[2] = {0, 0};
+        bool ok = true;
+        bool issued = false;
+        int k = 0;
+        for (int u = u_begin; ok && u < u_end; ++u, ++k) {
+          const UnitGeom g = unit_geom(a.units, u);
+          const uint32_t qb = 2 * (k & 1);
+          // Q tiles of this unit, prepared in both CTAs (and, for the first
+          // unit, the first K group landed in both)
+#pragma unroll
+          for (int s = 0; s < 2; ++s) {
+            if (!ok || s >= g.n_st) break;
+            ok = dev::mbar_wait(bars.q_ready(qb + s), q_use[qb + s] & 1, abort_flag, a.err, kTimeoutNs);
+            ++q_use[qb + s];
+          }
+          // this unit's first K tile: group 0, or the K half of the previous
+          // unit's last group (covered by that unit's last P-ready barrier)
+          const uint32_t k0 = k == 0 ? 0u : (kslot >= 2 ? kslot - 2 : kslot + kSlots - 2);
+          if (!ok) break;
+          dev::tc_fence_after();
+#pragma unroll
+          for (int s = 0; s < 2; ++s) {
+            if (s >= g.n_st) break;
+            issue_qk_f8(tmem + s * 128, sbase + C::SmemQ + (qb + s) * C::QTileBytes, sbase + C::SmemKV + k0 * C::SlotBytes);
+            dev::mma_commit_pair_mc(bars.s_ready(s, 0), kPairMask);
+            if (g.hi - g.lo == 1) dev::mma_commit_pair_mc(bars.q_empty(qb + s), kPairMask);
+          }
+          issued = true;
+          for (int j = g.lo; j < g.hi; ++j) {
+            // group grp = V(j) + the next K tile; its arrival in both CTAs is
+            // implied by P-ready of query tile 0
+            const bool more = j + 1 < g.hi;
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+              if (s >= g.n_st) break;
+              ok = dev::mbar_wait(bars.p_ready(s, 0), p_it[s] & 1, abort_flag, a.err, kTimeoutNs);
+              if (!ok) break;
+              ++p_it[s];
+              dev::tc_fence_after();
+              issue_pv_f8(tmem + 256 + s * 128, tmem + s * 128, sbase + C::SmemKV + vslot * C::SlotBytes, j > g.lo);
+              if (more) {
+                issue_qk_f8(tmem + s * 128, sbase + C::SmemQ + (qb + s) * C::QTileBytes,
+                            sbase + C::SmemKV + kslot * C::SlotBytes);
+                dev::mma_commit_pair_mc(bars.s_ready(s, 0), kPairMask);
+                if (j + 2 == g.hi) dev::mma_commit_pair_mc(bars.q_empty(qb + s), kPairMask);
+              } else {
+                dev::mma_commit_pair_mc(bars.pv_done(s, 0), kPairMask);  // the unit's O is complete
+              }
+            }
+            if (!ok) break;
+            vslot = vslot + 2 >= (uint32_t)kSlots ? vslot + 2 - kSlots : vslot + 2;
+            kslot = kslot + 2 >= (uint32_t)kSlots ? kslot + 2 - kSlots : kslot + 2;
+          }
+        }
+        if (!ok && issued) {
+          // drain: every MMA issued so far must finish before TMEM is freed
+          dev::mma_commit_pair(bars.drain());
+          dev::mbar_wait_bounded(bars.drain(), 0, nullptr, nullptr, kTimeoutNs);
+        }
+      }
+    } else if (rank == 0) {
+    // bf16: the whole warp runs the loop (its values stay warp-uniform); every
     // tcgen05 MMA and commit is issued by one elected lane.
-    if (rank == 0) {
       // ring slots of the current group's V and K halves: group n uses slots
       // 2n-1 and 2n (mod kSlots), advanced by two per key tile without a division
       uint32_t vslot = 1, kslot = 2, q_use[4] = {0, 0, 0, 0};
@@ -596,20 +666,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t d = tmem + s * 128 + h * 64;
         const uint32_t qa = sbase + C::SmemQ + qs * C::QTileBytes;
         const uint32_t kb = sbase + C::SmemKV + ks * C::SlotBytes + h * kHalfKeyRowsBytes;
-        if constexpr (kFp8)
-          issue_qk_f8(d, qa, kb);
-        else
-          issue_qk(d, qa, kb);
+        issue_qk(d, qa, kb);
         commit_pair_elect(bars.s_ready(s, h));
       };
       // PV of half h of the key tile whose V is in ring slot vs, query tile s
       auto pv_half = [&](int s, uint32_t vs, int h, bool acc) {
         const uint32_t d = tmem + 256 + s * 128, pt = tmem + s * 128 + h * 64;
         const uint32_t vb = sbase + C::SmemKV + vs * C::SlotBytes;
-        if constexpr (kFp8)
-          issue_pv_f8(d, pt, vb + 32 * h, acc);
-        else
-          issue_pv(d, pt, vb + 4096 * h, acc);
+        issue_pv(d, pt, vb + 4096 * h, acc);
       };
       // The first QK (half h) of query tile s of unit gg: Q slot qbase + s (its
       // readiness in both CTAs is awaited before half 0), K in ring slot ks.
@@ -782,136 +846,212 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int32_t row = g.q0 + st * 2 * kTileRows + (int32_t)rank * kTileRows + (int32_t)row_in_tile;
         if (row < a.S) sq_row = __ldg(a.sq + (int64_t)g.head * a.S + row);
       }
-      for (int j = g.lo; ok && j < g.hi; ++j) {
-        const uint32_t t = t_unit + (j - g.lo);  // the pair's running key-tile count
-        // score scale in log2 units: softmax_scale log2(e), times the q-row and
-        // key-tile scales for fp8
-        float rsc = sl2;
-        if constexpr (kFp8) rsc = sl2 * sq_row * __ldg(a.sk + (int64_t)g.head * a.S + g.kv0 + j * kTileRows);
-        const int rem = g.kv1 - (g.kv0 + j * kTileRows);
-        // fp8: test, without blocking, whether the next K/V group has landed;
-        // the blocking wait before half 0's P is reported then only runs if
-        // not (bf16 measured faster with the plain blocking wait)
-        const uint32_t kv_bar = bars.kv_full((t + 1) % kGroups), kv_par = ((t + 1) / kGroups) & 1;
-        const bool kv_landed = kFp8 && checks_kv && dev::mbar_test_wait(kv_bar, kv_par);
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          ok = dev::mbar_wait(bars.s_ready(st, h), s_it[h] & 1, abort_flag, a.err, kTimeoutNs);
+      if constexpr (kFp8) {
+        // FP8: whole 128-key tiles, one S phase per key tile.
+        for (int j = g.lo; j < g.hi; ++j) {
+          const uint32_t t = t_unit + (j - g.lo);  // the pair's running key-tile count
+          // score scale in log2 units: softmax_scale log2(e) times the q-row and key-tile scales
+          const float rsc = sl2 * sq_row * __ldg(a.sk + (int64_t)g.head * a.S + g.kv0 + j * kTileRows);
+          ok = dev::mbar_wait(bars.s_ready(st, 0), s_it[0] & 1, abort_flag, a.err, kTimeoutNs);
           if (!ok) break;
-          ++s_it[h];
-          // S half 1 of the last query tile is ready: every MMA before its QK is
-          // done, so the group holding K(t) (and V(t-1)) is free in this CTA
-          if (releases && h == 1) dev::mbar_arrive(bars.kv_empty(t % kGroups));
+          ++s_it[0];
+          // S of the last query tile is ready: every MMA before it is done, so
+          // the group holding K(t) (and V(t-1)) is free in this CTA
+          if (releases) dev::mbar_arrive(bars.kv_empty(t % kGroups));
+          // test, without blocking, whether the next K/V group has landed; the
+          // blocking wait below then only runs if it had not
+          const uint32_t kv_bar = bars.kv_full((t + 1) % kGroups), kv_par = ((t + 1) / kGroups) & 1;
+          const bool kv_landed = checks_kv && dev::mbar_test_wait(kv_bar, kv_par);
           __syncwarp();  // lanes leave the wait separately; the TMEM loads are warp-collective
           dev::tc_fence_after();
-          const uint32_t t_sh = t_s + 64 * h;  // this half's S, then its P
-          uint32_t r[2][32];
-          dev::tmem_ld32(t_sh, r[0]);
-          dev::tmem_ld32(t_sh + 32, r[1]);
-          dev::tmem_wait_ld();
-          float sv[64];
-#pragma unroll
-          for (int c = 0; c < 64; ++c) sv[c] = __uint_as_float(r[c >> 5][c & 31]);
-          if (rem < kTileRows) {
-#pragma unroll
-            for (int c = 0; c < 64; ++c)
-              if (half_key(c, h) >= rem) sv[c] = -INFINITY;
-          }
-          // Row max of the half: eight independent chains of 3-input maxima.
+          uint32_t r[4][32];
+          float* sv = reinterpret_cast<float*>(&r[0][0]);
+          const int rem = g.kv1 - (g.kv0 + j * kTileRows);
+          load_scores128(t_s, r, rem);
+          // Row max: eight independent chains of 3-input maxima.
           float mx[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) mx[i] = fmaxf(sv[i], sv[8 + i]);
 #pragma unroll
-          for (int c = 16; c < 64; c += 16)
+          for (int c = 16; c < 128; c += 16)
 #pragma unroll
             for (int i = 0; i < 8; ++i) mx[i] = dev::max3(mx[i], sv[c + i], sv[c + 8 + i]);
           const float m_new =
               dev::max3(dev::max3(mx[0], mx[1], mx[2]), dev::max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * rsc;
           // The reference max only moves when the row max grows by more than
-          // 2^8 (then O and l are rescaled; the final O / l is unchanged).
+          // 2^8 (then O and l are rescaled; the final O / l is unchanged).  The
+          // O row is rescaled after P is written: the next PV waits for p_ready.
           float alpha = 1.f;
           if (m_new > m_used + kRescaleThreshold) {
-            alpha = dev::ex2_approx(m_used - m_new);  // 0 on the first half of a unit (m_used = -inf)
+            alpha = dev::ex2_approx(m_used - m_new);  // 0 on the first tile (m_used = -inf)
             m_used = m_new;
           }
           const float neg = -m_used;
           float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-          uint32_t p[32];
 #pragma unroll
-          for (int c = 0; c < 32; ++c) {
-            // packed pair arithmetic: one f32x2 FMA for the exponents, one f32x2 add for the sums
-            float x0, x1;
-            dev::fma2(x0, x1, sv[2 * c], sv[2 * c + 1], rsc, rsc, neg, neg);
-            const float p0 = dev::ex2_approx(x0), p1 = dev::ex2_approx(x1);
-            const int ai = 2 * (c & 3);
-            dev::add2(rs8[ai], rs8[ai + 1], rs8[ai], rs8[ai + 1], p0, p1);
-            if constexpr (kFp8) {
+          for (int h = 0; h < 2; ++h) {
+            uint32_t p[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              // packed pair arithmetic: one f32x2 FMA for the exponents, one f32x2 add for the sums
+              float x0, x1;
+              dev::fma2(x0, x1, sv[64 * h + 2 * c], sv[64 * h + 2 * c + 1], rsc, rsc, neg, neg);
+              const float p0 = dev::ex2_approx(x0), p1 = dev::ex2_approx(x1);
+              const int ai = 2 * (c & 3);
+              dev::add2(rs8[ai], rs8[ai + 1], rs8[ai], rs8[ai + 1], p0, p1);
               // e4m3, four per column (p <= 2^8 < 448: no scale)
               const uint32_t two = e4m3x2(p0, p1);
               p[c >> 1] = (c & 1) ? (p[c >> 1] | (two << 16)) : two;
-            } else {
-              p[c] = dev::pack_bf16x2(p0, p1);
             }
-          }
-          if constexpr (kFp8) {
             uint32_t p16[16];
 #pragma unroll
             for (int i = 0; i < 16; ++i) p16[i] = p[i];
-            dev::tmem_st16(t_sh, p16);
-          } else {
-            dev::tmem_st32(t_sh, p);
+            dev::tmem_st16(t_s + 16 * h, p16);
           }
           const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
           l = l * alpha + rs;
           // tcgen05.ld/st are warp-collective (.sync.aligned): the rescale runs
           // for the whole warp when any of its rows needs it (alpha = 1
-          // elsewhere).  The PV of the previous half (the other half) may
-          // still be adding into O (every earlier PV of this tile completed
-          // before the QK whose S was just read), so it is awaited first: the
-          // QK issued right after it fills the other half's next S, which this
-          // thread reads next anyway; in the last key tile no such QK may
-          // follow, and "PV done" of half 0 is awaited instead.
-          if (!(j == g.lo && h == 0) && __any_sync(0xffffffffu, alpha != 1.f)) {
-            if (h == 1 && j + 1 == g.hi)
-              ok = dev::mbar_wait(bars.pv_done(st, 0), n_done & 1, abort_flag, a.err, kTimeoutNs);
-            else
-              ok = dev::mbar_wait(bars.s_ready(st, 1 - h), s_it[1 - h] & 1, abort_flag, a.err, kTimeoutNs);
-            __syncwarp();
-            dev::tc_fence_after();
-#pragma unroll 1
-            for (int c = 0; c < 8; ++c) {
-              uint32_t ov[16];
-              dev::tmem_ld16(t_o + c * 16, ov);
+          // elsewhere); every MMA before the QK just read (PV(t-1) included)
+          // has completed.
+          if (j > g.lo && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              uint32_t ov[32];
+              dev::tmem_ld32(t_o + c * 32, ov);
               dev::tmem_wait_ld();
 #pragma unroll
-              for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
-              dev::tmem_st16(t_o + c * 16, ov);
+              for (int e = 0; e < 32; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+              dev::tmem_st32(t_o + c * 32, ov);
             }
           }
           dev::tmem_wait_st();
           dev::tc_fence_before();
           __syncwarp();
-          // half 0's PV reads V(t) and the QK after it K(t+1): group t+1 must have
-          // landed in this CTA before query tile 0 reports that P ready
-          if (h == 0 && checks_kv && (kFp8 ? !kv_landed : true))
-            ok = dev::mbar_wait(kv_bar, kv_par, abort_flag, a.err, kTimeoutNs) && ok;
+          // the next PV reads V(t) and the QK after it K(t+1): group t+1 must have
+          // landed in this CTA before query tile 0 reports P ready
+          if (checks_kv && !kv_landed) ok = dev::mbar_wait(kv_bar, kv_par, abort_flag, a.err, kTimeoutNs);
           if (lane == 0) {  // P (and O) of the warp's 32 rows
-            if (kFp8 && rank == 0)  // fp8: the even CTA's own barrier, arrived on locally
-              dev::mbar_arrive(bars.p_ready(st, h));
+            if (rank == 0)
+              dev::mbar_arrive(bars.p_ready(st, 0));  // the even CTA's own barrier, arrived on locally
             else
-              dev::mbar_arrive_cluster(p_ready_remote[h]);
+              dev::mbar_arrive_cluster(p_ready_remote[0]);
           }
           if (!__all_sync(0xffffffffu, ok)) {
             ok = false;
             break;
           }
         }
+      } else {
+        // bf16: 64-key halves (see the kernel header).
+        for (int j = g.lo; ok && j < g.hi; ++j) {
+          const uint32_t t = t_unit + (j - g.lo);  // the pair's running key-tile count
+          const float rsc = sl2;  // score scale in log2 units: softmax_scale log2(e)
+          const int rem = g.kv1 - (g.kv0 + j * kTileRows);
+          const uint32_t kv_bar = bars.kv_full((t + 1) % kGroups), kv_par = ((t + 1) / kGroups) & 1;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            ok = dev::mbar_wait(bars.s_ready(st, h), s_it[h] & 1, abort_flag, a.err, kTimeoutNs);
+            if (!ok) break;
+            ++s_it[h];
+            // S half 1 of the last query tile is ready: every MMA before its QK is
+            // done, so the group holding K(t) (and V(t-1)) is free in this CTA
+            if (releases && h == 1) dev::mbar_arrive(bars.kv_empty(t % kGroups));
+            __syncwarp();  // lanes leave the wait separately; the TMEM loads are warp-collective
+            dev::tc_fence_after();
+            const uint32_t t_sh = t_s + 64 * h;  // this half's S, then its P
+            uint32_t r[2][32];
+            dev::tmem_ld32(t_sh, r[0]);
+            dev::tmem_ld32(t_sh + 32, r[1]);
+            dev::tmem_wait_ld();
+            float sv[64];
+#pragma unroll
+            for (int c = 0; c < 64; ++c) sv[c] = __uint_as_float(r[c >> 5][c & 31]);
+            if (rem < kTileRows) {
+#pragma unroll
+              for (int c = 0; c < 64; ++c)
+                if (half_key(c, h) >= rem) sv[c] = -INFINITY;
+            }
+            // Row max of the half: eight independent chains of 3-input maxima.
+            float mx[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) mx[i] = fmaxf(sv[i], sv[8 + i]);
+#pragma unroll
+            for (int c = 16; c < 64; c += 16)
+#pragma unroll
+              for (int i = 0; i < 8; ++i) mx[i] = dev::max3(mx[i], sv[c + i], sv[c + 8 + i]);
+            const float m_new =
+                dev::max3(dev::max3(mx[0], mx[1], mx[2]), dev::max3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7])) * rsc;
+            // The reference max only moves when the row max grows by more than
+            // 2^8 (then O and l are rescaled; the final O / l is unchanged).
+            float alpha = 1.f;
+            if (m_new > m_used + kRescaleThreshold) {
+              alpha = dev::ex2_approx(m_used - m_new);  // 0 on the first half of a unit (m_used = -inf)
+              m_used = m_new;
+            }
+            const float neg = -m_used;
+            float rs8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            uint32_t p[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+              // packed pair arithmetic: one f32x2 FMA for the exponents, one f32x2 add for the sums
+              float x0, x1;
+              dev::fma2(x0, x1, sv[2 * c], sv[2 * c + 1], rsc, rsc, neg, neg);
+              const float p0 = dev::ex2_approx(x0), p1 = dev::ex2_approx(x1);
+              const int ai = 2 * (c & 3);
+              dev::add2(rs8[ai], rs8[ai + 1], rs8[ai], rs8[ai + 1], p0, p1);
+              p[c] = dev::pack_bf16x2(p0, p1);
+            }
+            dev::tmem_st32(t_sh, p);
+            const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
+            l = l * alpha + rs;
+            // tcgen05.ld/st are warp-collective (.sync.aligned): the rescale runs
+            // for the whole warp when any of its rows needs it (alpha = 1
+            // elsewhere).  The PV of the previous half (the other half) may
+            // still be adding into O (every earlier PV of this tile completed
+            // before the QK whose S was just read), so it is awaited first: the
+            // QK issued right after it fills the other half's next S, which this
+            // thread reads next anyway; in the last key tile no such QK may
+            // follow, and "PV done" of half 0 is awaited instead.
+            if (!(j == g.lo && h == 0) && __any_sync(0xffffffffu, alpha != 1.f)) {
+              if (h == 1 && j + 1 == g.hi)
+                ok = dev::mbar_wait(bars.pv_done(st, 0), n_done & 1, abort_flag, a.err, kTimeoutNs);
+              else
+                ok = dev::mbar_wait(bars.s_ready(st, 1 - h), s_it[1 - h] & 1, abort_flag, a.err, kTimeoutNs);
+              __syncwarp();
+              dev::tc_fence_after();
+#pragma unroll 1
+              for (int c = 0; c < 8; ++c) {
+                uint32_t ov[16];
+                dev::tmem_ld16(t_o + c * 16, ov);
+                dev::tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) ov[e] = __float_as_uint(__uint_as_float(ov[e]) * alpha);
+                dev::tmem_st16(t_o + c * 16, ov);
+              }
+            }
+            dev::tmem_wait_st();
+            dev::tc_fence_before();
+            __syncwarp();
+            // half 0's PV reads V(t) and the QK after it K(t+1): group t+1 must have
+            // landed in this CTA before query tile 0 reports that P ready
+            // (a blocking wait and the cluster-address arrive measured faster here
+            // than FP8's non-blocking test and local arrive)
+            if (h == 0 && checks_kv) ok = dev::mbar_wait(kv_bar, kv_par, abort_flag, a.err, kTimeoutNs) && ok;
+            if (lane == 0) dev::mbar_arrive_cluster(p_ready_remote[h]);  // P (and O) of the warp's 32 rows
+            if (!__all_sync(0xffffffffu, ok)) {
+              ok = false;
+              break;
+            }
+          }
+        }
       }
       if (!ok) break;
       // the unit's last PVs of this query tile, one per half ("PV done" of a
-      // half completes once per unit, after its last key tile's PV)
+      // half completes once per unit, after its last key tile's PV; FP8: one,
+      // after the unit's last PV)
       ok = dev::mbar_wait(bars.pv_done(st, 0), n_done & 1, abort_flag, a.err, kTimeoutNs) &&
-           dev::mbar_wait(bars.pv_done(st, 1), n_done & 1, abort_flag, a.err, kTimeoutNs);
+           (kFp8 || dev::mbar_wait(bars.pv_done(st, 1), n_done & 1, abort_flag, a.err, kTimeoutNs));
       ++n_done;
       if (!ok) break;
       __syncwarp();
