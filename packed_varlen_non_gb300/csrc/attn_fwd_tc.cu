@@ -852,6 +852,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t t = t_unit + (j - g.lo);  // the pair's running key-tile count
           // score scale in log2 units: softmax_scale log2(e) times the q-row and key-tile scales
           const float rsc = sl2 * sq_row * __ldg(a.sk + (int64_t)g.head * a.S + g.kv0 + j * kTileRows);
+          // (every lane runs the same bounded wait on the same barrier, timer and
+          // abort flag in step, so the warp leaves it with one value of ok)
           ok = dev::mbar_wait(bars.s_ready(st, 0), s_it[0] & 1, abort_flag, a.err, kTimeoutNs);
           if (!ok) break;
           ++s_it[0];
@@ -951,8 +953,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t kv_bar = bars.kv_full((t + 1) % kGroups), kv_par = ((t + 1) / kGroups) & 1;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            ok = dev::mbar_wait(bars.s_ready(st, h), s_it[h] & 1, abort_flag, a.err, kTimeoutNs);
-            if (!ok) break;
+            // (no lane leaves here: a failed wait only clears ok, and the
+            // warp-uniform vote at the end of the half ends the loop)
+            ok = dev::mbar_wait(bars.s_ready(st, h), s_it[h] & 1, abort_flag, a.err, kTimeoutNs) && ok;
             ++s_it[h];
             // S half 1 of the last query tile is ready: every MMA before its QK is
             // done, so the group holding K(t) (and V(t-1)) is free in this CTA
@@ -1015,9 +1018,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // follow, and "PV done" of half 0 is awaited instead.
             if (!(j == g.lo && h == 0) && __any_sync(0xffffffffu, alpha != 1.f)) {
               if (h == 1 && j + 1 == g.hi)
-                ok = dev::mbar_wait(bars.pv_done(st, 0), n_done & 1, abort_flag, a.err, kTimeoutNs);
+                ok = dev::mbar_wait(bars.pv_done(st, 0), n_done & 1, abort_flag, a.err, kTimeoutNs) && ok;
               else
-                ok = dev::mbar_wait(bars.s_ready(st, 1 - h), s_it[1 - h] & 1, abort_flag, a.err, kTimeoutNs);
+                ok = dev::mbar_wait(bars.s_ready(st, 1 - h), s_it[1 - h] & 1, abort_flag, a.err, kTimeoutNs) && ok;
               __syncwarp();
               dev::tc_fence_after();
 #pragma unroll 1
@@ -1053,7 +1056,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       ok = dev::mbar_wait(bars.pv_done(st, 0), n_done & 1, abort_flag, a.err, kTimeoutNs) &&
            (kFp8 || dev::mbar_wait(bars.pv_done(st, 1), n_done & 1, abort_flag, a.err, kTimeoutNs));
       ++n_done;
-      if (!ok) break;
+      // every lane of a bf16 warp leaves together (FP8's lanes run the bounded
+      // waits in step; its loop is sensitive to code shape)
+      if constexpr (kFp8) {
+        if (!ok) break;
+      } else if (!__all_sync(0xffffffffu, ok)) {
+        break;
+      }
       __syncwarp();
       dev::tc_fence_after();
       const int32_t local = st * 2 * kTileRows + (int32_t)rank * kTileRows + (int32_t)row_in_tile;
