@@ -1133,18 +1133,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // Combines the pieces of units split along the keys: one warp per query row,
 // four dims per lane.  With M = max_c m_c (log2 units):
 //   o = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c,  lse = (M + log2 l) ln 2.
-__global__ void __launch_bounds__(256) attn_merge_kernel(ForwardArgs a) {
+// At 32 registers a thread, eight blocks fit on an SM, so the rows of a
+// typical last round (a few thousand warps) run in one wave.  It is launched
+// as a programmatic dependent of the forward: its blocks are scheduled as the
+// forward's CTAs leave and wait here for the forward's writes.
+__global__ void __launch_bounds__(256, 8) attn_merge_kernel(ForwardArgs a) {
   const int warp_global = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   const int mu = warp_global / kUnitRows, r = warp_global % kUnitRows;
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the forward is complete and its writes visible
   if (mu >= a.n_merges) return;
   const MergeUnit m = a.merges[mu];
   const int32_t row = m.q_row0 + r;
   if (row >= m.kv_end) return;
   float M = -INFINITY;
+#pragma unroll 4
   for (int c = 0; c < m.n_parts; ++c) M = fmaxf(M, a.part_ml[(size_t)(m.part0 + c) * kUnitRows + r].x);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float l = 0.f;
+#pragma unroll 4
   for (int c = 0; c < m.n_parts; ++c) {
     const size_t slot = (size_t)(m.part0 + c) * kUnitRows + r;
     const float2 ml = a.part_ml[slot];
@@ -1228,8 +1235,18 @@ cudaError_t launch_pairs(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
   e = cudaGetLastError();
   if (e != cudaSuccess || a.n_merges == 0) return e;
   const int64_t warps = (int64_t)a.n_merges * kUnitRows;
-  attn_merge_kernel<<<(int)((warps + 7) / 8), 256, 0, stream>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((warps + 7) / 8));
+  cfg.blockDim = dim3(256);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, attn_merge_kernel, a);
+  if (e != cudaSuccess && why) *why = "the merge launch failed";
+  return e;
 }
 
 }  // namespace
