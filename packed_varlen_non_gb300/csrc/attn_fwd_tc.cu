@@ -16,14 +16,15 @@
 // K tile and dims [64 rank, 64 rank + 64) of a V tile -- so a CTA reads
 // (and loads from L2) half the key/value bytes a single-CTA kernel would.
 // Per CTA, 11 warps:
-//   warp 9       TMA producer: its own Q tiles (double buffered: the next
-//                unit's behind the current unit's first K/V group), and its
-//                halves of the document's K and V tiles through a 6-slot ring;
-//                V(j) and the next K tile form one group behind one barrier.
-//   warp 10      Q warp: as each Q tile lands, applies the fused Q prologue
+//   warp 9       TMA producer: its halves of the document's K and V tiles
+//                through a 6-slot ring; V(j) and the next K tile form one
+//                group behind one barrier.  (FP8: also its own Q tiles, the
+//                next unit's behind the current unit's first K/V group.)
+//   warp 10      Q warp: loads this CTA's Q tiles (bf16) into double-buffered
+//                slots as they come free, so the next unit's tiles are ready
+//                before it starts; as each lands, applies the fused Q prologue
 //                in place when asked (RMSNorm with gain, rot96 rotation) and
-//                reports the tile ready to the even CTA.  Q tiles are double
-//                buffered, so the next unit's tiles are ready before it starts.
+//                reports the tile ready to the even CTA.
 //   warp 8       even CTA: MMA issuer for the pair, S = Q_s K^T and
 //                O_s += P V, fp32 accumulators in TMEM.  Both CTAs' warp 8
 //                allocate the pair's TMEM together.
@@ -32,7 +33,11 @@
 //                S row from TMEM, keeps the running max and sum in registers,
 //                writes P as bf16 back into TMEM over its S columns, rescales
 //                its O row when the max has grown by more than 2^8, and at the
-//                end of the unit writes O / l and the log-sum-exp.
+//                end of the unit writes O / l and the log-sum-exp.  A bf16
+//                warp whose 32 rows all lie in the document stages them in
+//                the unit's Q slot (free once the unit's MMAs are done) and
+//                sends them out with two TMA tile stores, then frees the slot
+//                for the Q warp; other warps store their rows directly.
 // Each 128-key tile is taken in two halves of 64 keys, h = 0, 1, each with
 // its own 64 TMEM columns of S: per query tile the issuer runs PV of half h
 // of key tile j and then QK of half h of key tile j + 1 into the same
@@ -62,7 +67,7 @@
 // K-major operands; V is the MN-major B operand of the PV product.
 //
 // Barriers: completion of the pair's MMAs is multicast to both CTAs (S half
-// ready, PV done, Q slots free).  The MMA-issuing thread paces the tensor
+// ready, PV done; FP8: Q slots free).  The MMA-issuing thread paces the tensor
 // cores, so per key-tile half it only waits for P and commits: its "P ready"
 // barrier of (query tile, half) counts one arrival per softmax warp of both
 // CTAs, and softmax warp 0 of each CTA reports half 0 only once its CTA's next
@@ -74,7 +79,8 @@
 // waits for the other half's latest PV: through the S-ready of the QK issued
 // right after it, or "PV done" in the last key tile.  Q tiles:
 // the even CTA's "Q ready" barrier counts one arrival from the Q warp of each
-// CTA.
+// CTA; a bf16 Q slot's "free" barrier counts the four softmax warps of its
+// query tile in that CTA, after their epilogue.
 //
 // FP8 variant (template argument kFp8, h3attn_forward_fp8): the same kernel
 // on e4m3 Q, K and transposed V (channel rows of keys, every document
@@ -95,6 +101,7 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "device_common.cuh"
@@ -451,7 +458,8 @@ static __device__ __noinline__ void norm_rope_q_row(uint32_t tile, uint32_t r, c
 template <bool kFp8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                       const __grid_constant__ CUtensorMap tm_v, ForwardArgs a) {
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                       ForwardArgs a, int o_tma) {
   using C = Cfg<kFp8>;
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = dev::smem_u32(smem_raw);
@@ -472,7 +480,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     for (int i = 0; i < 4; ++i) {
       dev::mbar_init(bars.q_full(i), 1);
-      dev::mbar_init(bars.q_empty(i), 1);
+      // FP8: freed by the MMA issuer after a unit's last QK; bf16: by the four
+      // softmax warps of the tile in each CTA, after their epilogue (which
+      // stages the O tile in the finished unit's Q slot)
+      dev::mbar_init(bars.q_empty(i), kFp8 ? 1 : 4);
       dev::mbar_init(bars.q_ready(i), 2);           // the Q warp of each CTA of the pair
     }
     for (int s = 0; s < 2; ++s) {
@@ -512,8 +523,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t pol_kv = dev::policy_evict_last();
       uint32_t grp = 0, q_use[4] = {0, 0, 0, 0};
       bool ok = true;
-      // Q tiles of the unit with ordinal k, into buffer k & 1 (the slot is
-      // freed by the MMA after the last QK of the unit two before).
+      // FP8: Q tiles of the unit with ordinal k, into buffer k & 1 (the slot
+      // is freed by the MMA after the last QK of the unit two before).
       auto load_q = [&](const UnitGeom& g, int k) {
 #pragma unroll
         for (int s = 0; s < 2; ++s) {
@@ -539,7 +550,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // unit's first K tile -- in slots (2n-1) % kSlots and 2n % kSlots, one
         // full and one empty barrier (index n % kGroups) for both.
         if (k == 0) {
-          load_q(g, 0);
+          if constexpr (kFp8) load_q(g, 0);
           if (!ok) break;
           ok = dev::mbar_wait(bars.kv_empty(0), 1, abort_flag, a.err, kTimeoutNs);
           if (!ok) break;
@@ -569,7 +580,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                               k_head, k_row, rank, pol_kv);
           ++grp;
           // the next unit's Q tiles, behind this unit's first group
-          if (j == g.lo && has_next) load_q(unit_geom(a.units, u + 1), k + 1);
+          if constexpr (kFp8)
+            if (j == g.lo && has_next) load_q(unit_geom(a.units, u + 1), k + 1);
         }
       }
       if (!ok) {
@@ -686,7 +698,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           dev::tc_fence_after();
         }
         qk_half(s, qbase + s, ks, h);
-        if (h == 1 && gg.hi - gg.lo == 1) commit_pair_elect(bars.q_empty(qbase + s));
         issued = true;
       };
       for (int u = u_begin; ok && u < u_end; ++u, ++k) {
@@ -716,7 +727,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // steady state: key tiles with a next key tile in this unit
         for (int j = g.lo; ok && j + 1 < g.hi; ++j) {
           const bool acc0 = j > g.lo;
-          const bool last_qk = j + 2 == g.hi;  // QK(., j + 1, 1) is the unit's last QK of the tile
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
 #pragma unroll
@@ -731,7 +741,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               dev::tc_fence_after();
               pv_half(s, vslot, h, acc0 || h == 1);
               qk_half(s, qb + s, kslot, h);
-              if (h == 1 && last_qk) commit_pair_elect(bars.q_empty(qb + s));
             }
             if (!ok) break;
           }
@@ -786,13 +795,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t q_use[4] = {0, 0, 0, 0};
     bool ok = true;
     const bool fuse_q = a.gain_q != nullptr;
+    const uint64_t pol_q = dev::policy_evict_first();
     int k = 0;
     for (int u = u_begin; ok && u < u_end; ++u, ++k) {
       const UnitGeom g = unit_geom(a.units, u);
 #pragma unroll 1
       for (int s = 0; s < 2 && s < g.n_st; ++s) {
         const int i = 2 * (k & 1) + s;
-        bool good = dev::mbar_wait(bars.q_full(i), q_use[i] & 1, abort_flag, a.err, kTimeoutNs);
+        bool good = true;
+        if constexpr (!kFp8) {
+          // bf16: this warp loads the tile once its slot is free (the
+          // previous unit in the slot has finished its epilogue)
+          if (lane == 0) {
+            good = dev::mbar_wait(bars.q_empty(i), (q_use[i] & 1) ^ 1, abort_flag, a.err, kTimeoutNs);
+            if (good) {
+              const uint32_t dst = sbase + C::SmemQ + i * C::QTileBytes;
+              const int32_t row = g.q0 + s * 2 * kTileRows + (int32_t)rank * kTileRows;
+              dev::mbar_arrive_expect_tx(bars.q_full(i), C::QTileBytes);
+              dev::tma_load_2d(dst, &tm_q, bars.q_full(i), g.head * 128, row, pol_q);
+              dev::tma_load_2d(dst + kQHalfBytes, &tm_q, bars.q_full(i), g.head * 128 + 64, row, pol_q);
+            }
+          }
+          good = __shfl_sync(0xffffffffu, good, 0);
+          if (!good) {
+            ok = false;
+            break;
+          }
+        }
+        good = dev::mbar_wait(bars.q_full(i), q_use[i] & 1, abort_flag, a.err, kTimeoutNs);
         ++q_use[i];
         if (!kFp8 && good && fuse_q) {
           const int32_t row0 = g.q0 + s * 2 * kTileRows + (int32_t)rank * kTileRows;
@@ -811,6 +841,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) dev::mbar_arrive_cluster(dev::mapa_shared(bars.q_ready(i), 0));
         ok = __all_sync(0xffffffffu, good);
         if (!ok) break;
+      }
+    }
+    if constexpr (!kFp8) {
+      if (!ok && lane == 0) {
+        // drain: wait (bounded) for the Q copies this warp issued
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (q_use[i]) dev::mbar_wait_bounded(bars.q_full(i), (q_use[i] - 1) & 1, nullptr, nullptr, kTimeoutNs);
       }
     }
   } else {
@@ -836,6 +874,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const uint32_t t_unit = t0;
       t0 += g.hi - g.lo;
       if (st >= g.n_st) continue;
+      const uint32_t q_slot = 2 * ((u - u_begin) & 1) + st;  // this unit's Q tile of this query tile
       // ring bookkeeping by one lane of one warp per CTA
       const bool releases = lead_lane && st == g.n_st - 1;
       const bool checks_kv = lead_lane && st == 0;
@@ -1088,29 +1127,74 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
         if (valid) a.part_ml[slot] = make_float2(m_used, l);
+        if constexpr (!kFp8) {
+          __syncwarp();
+          if (lane == 0) dev::mbar_arrive(bars.q_empty(q_slot));
+        }
         continue;
       }
       const float inv = 1.f / l;
-      __nv_bfloat16* dst = og + (int64_t)row * a.o_stride + g.head * kHeadDim;
+      bool staged = false;
+      if constexpr (!kFp8) staged = o_tma != 0 && __all_sync(0xffffffffu, valid);
+      if (staged) {
+        // The warp's 32 rows, bf16, into its rows of the unit's Q slot (free:
+        // every MMA of the unit is done) in the tile's 128-byte swizzled
+        // layout, then two TMA stores (dims 0..63, 64..127) of 32 rows each.
+        const uint32_t tile = sbase + C::SmemQ + q_slot * C::QTileBytes;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t ov[32];
-        dev::tmem_ld32(t_o + c * 32, ov);
-        dev::tmem_wait_ld();
-        if constexpr (kFp8) scale_by_channel(ov, a.sv + g.head * kHeadDim + c * 32);
-        if (valid) {
+        for (int c = 0; c < 4; ++c) {
+          uint32_t ov[32];
+          dev::tmem_ld32(t_o + c * 32, ov);
+          dev::tmem_wait_ld();
           uint32_t w[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e)
             w[e] = dev::pack_bf16x2(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
-          if (o_wide) {  // rows and chunks 32-byte aligned: two 32-byte stores per chunk
-            dev::st_global_v8(dst + c * 32, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
-            dev::st_global_v8(dst + c * 32 + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
-          } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              *reinterpret_cast<uint4*>(dst + c * 32 + e * 8) = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t cc = 4 * c + e;  // 16-byte chunk of the row
+            const uint32_t addr = tile + (cc >> 3) * kQHalfBytes + row_in_tile * 128u + (((cc & 7u) ^ (row_in_tile & 7u)) << 4);
+            asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[4 * e]), "r"(w[4 * e + 1]),
+                         "r"(w[4 * e + 2]), "r"(w[4 * e + 3])
+                         : "memory");
           }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the TMA unit
+        __syncwarp();
+        if (lane == 0) {
+          const int32_t row0 = g.q0 + st * 2 * kTileRows + (int32_t)rank * kTileRows + (int32_t)lane_base;
+          dev::tma_store_2d(&tm_o, tile + lane_base * 128u, g.head * kHeadDim, row0);
+          dev::tma_store_2d(&tm_o, tile + kQHalfBytes + lane_base * 128u, g.head * kHeadDim + 64, row0);
+          dev::bulk_commit();
+          dev::bulk_wait_read_all();  // the slot is read: the next unit's Q may land there
+          dev::mbar_arrive(bars.q_empty(q_slot));
+        }
+      } else {
+        __nv_bfloat16* dst = og + (int64_t)row * a.o_stride + g.head * kHeadDim;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t ov[32];
+          dev::tmem_ld32(t_o + c * 32, ov);
+          dev::tmem_wait_ld();
+          if constexpr (kFp8) scale_by_channel(ov, a.sv + g.head * kHeadDim + c * 32);
+          if (valid) {
+            uint32_t w[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              w[e] = dev::pack_bf16x2(__uint_as_float(ov[2 * e]) * inv, __uint_as_float(ov[2 * e + 1]) * inv);
+            if (o_wide) {  // rows and chunks 32-byte aligned: two 32-byte stores per chunk
+              dev::st_global_v8(dst + c * 32, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
+              dev::st_global_v8(dst + c * 32 + 16, w[8], w[9], w[10], w[11], w[12], w[13], w[14], w[15]);
+            } else {
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                *reinterpret_cast<uint4*>(dst + c * 32 + e * 8) = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+            }
+          }
+        }
+        if constexpr (!kFp8) {
+          __syncwarp();
+          if (lane == 0) dev::mbar_arrive(bars.q_empty(q_slot));
         }
       }
       if (valid && a.lse != nullptr)
@@ -1118,6 +1202,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   }
 
+  if constexpr (!kFp8)
+    if (warp < kMmaWarp && lane == 0) dev::bulk_wait_all();  // the epilogue's TMA stores are complete
   // Neither CTA leaves (or frees the pair's TMEM) while the other may still
   // arrive on its barriers or run MMAs on its shared memory and TMEM.
   dev::tc_fence_before();
@@ -1218,8 +1304,9 @@ cudaError_t set_smem_attr() {
 }
 
 template <bool kFp8>
-cudaError_t launch_pairs(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const ForwardArgs& a,
-                         int device, int num_sms, cudaStream_t stream, std::string* why) {
+cudaError_t launch_pairs(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mo,
+                         int o_tma, const ForwardArgs& a, int device, int num_sms, cudaStream_t stream,
+                         std::string* why) {
   cudaError_t e = set_smem_attr<kFp8>();
   if (e != cudaSuccess) {
     if (why) *why = "cudaFuncSetAttribute(max dynamic shared memory) failed";
@@ -1231,7 +1318,7 @@ cudaError_t launch_pairs(const CUtensorMap& mq, const CUtensorMap& mk, const CUt
     if (why) *why = "the work list has no CTA pairs";
     return cudaErrorInvalidValue;
   }
-  attn_fwd_tc_kernel<kFp8><<<2 * a.n_pairs, kThreads, Cfg<kFp8>::SmemAlloc, stream>>>(mq, mk, mv, a);
+  attn_fwd_tc_kernel<kFp8><<<2 * a.n_pairs, kThreads, Cfg<kFp8>::SmemAlloc, stream>>>(mq, mk, mv, mo, a, o_tma);
   e = cudaGetLastError();
   if (e != cudaSuccess || a.n_merges == 0) return e;
   const int64_t warps = (int64_t)a.n_merges * kUnitRows;
@@ -1285,7 +1372,14 @@ cudaError_t launch_forward(const ForwardArgs& a, int device, int num_sms, cudaSt
       !make_map(&mk, a.k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, a.S, row, kTileRows / 2, why) ||
       !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, a.S, row, kTileRows, why))
     return cudaErrorInvalidValue;
-  return launch_pairs<false>(mq, mk, mv, a, device, num_sms, stream, why);
+  // O tiles go out by TMA when its rows allow a tensor map (16-byte aligned
+  // base and row stride); otherwise the epilogue stores them directly
+  CUtensorMap mo;
+  std::memset(&mo, 0, sizeof(mo));
+  const bool o_tma = (reinterpret_cast<uintptr_t>(a.o) & 15u) == 0 && (a.o_stride & 7) == 0 &&
+                     make_map(&mo, a.o, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, inner, a.S, (uint64_t)a.o_stride * 2, 32,
+                              nullptr);
+  return launch_pairs<false>(mq, mk, mv, mo, o_tma ? 1 : 0, a, device, num_sms, stream, why);
 }
 
 cudaError_t launch_forward_fp8(const ForwardArgs& a, int device, int num_sms, cudaStream_t stream,
@@ -1299,7 +1393,9 @@ cudaError_t launch_forward_fp8(const ForwardArgs& a, int device, int num_sms, cu
       !make_map(&mv, a.v, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, a.v_row_bytes, inner, a.v_row_bytes, kTileRows / 2,
                 why))
     return cudaErrorInvalidValue;
-  return launch_pairs<true>(mq, mk, mv, a, device, num_sms, stream, why);
+  CUtensorMap mo;
+  std::memset(&mo, 0, sizeof(mo));
+  return launch_pairs<true>(mq, mk, mv, mo, 0, a, device, num_sms, stream, why);
 }
 
 }  // namespace h3

@@ -351,6 +351,19 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
   return m;
 }
 
+// 2D tiled bulk-tensor store shared -> global, tracked by this thread's bulk
+// groups; commit, and waits until the groups have read their shared memory
+// (.read) or are complete.
+__device__ __forceinline__ void tma_store_2d(const void* desc, uint32_t src, int32_t c0, int32_t c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(desc)),
+               "r"(src), "r"(c0), "r"(c1)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 // Packed pair arithmetic on two fp32 lanes (one instruction each on sm_100
 // and later): (d0, d1) = (a0*b0 + c0, a1*b1 + c1) and (a0 + b0, a1 + b1).
 __device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0, float b1,

@@ -186,9 +186,11 @@ def test_running_max_jump_rescales_o(lib, col):
 @pytest.mark.parametrize("offset,pad", [(8, 0), (0, 8), (8, 8)])
 def test_output_alignments_are_byte_identical(lib, offset, pad):
     # o starting 16 bytes past a 32-byte boundary and/or a row stride that is a
-    # multiple of 8 but not of 16 elements: the epilogue's 16-byte stores
-    # instead of its 32-byte ones, same bytes.  Ragged documents and a split
-    # last wave (units that write partial results) included.
+    # multiple of 8 but not of 16 elements: the same bytes from the epilogue's
+    # TMA tile stores (warps whose rows all lie in their document) and from its
+    # direct stores (warps at a document end), which take 16-byte stores
+    # instead of 32-byte ones here.  Ragged documents and a split last wave
+    # (units that write partial results) included.
     lens = [1000, 3, 513, 129, 1]
     Hh = 3
     S, W = sum(lens), Hh * 128
