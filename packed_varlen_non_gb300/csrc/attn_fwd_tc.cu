@@ -36,8 +36,10 @@
 //                end of the unit writes O / l and the log-sum-exp.  A bf16
 //                warp whose 32 rows all lie in the document stages them in
 //                the unit's Q slot (free once the unit's MMAs are done) and
-//                sends them out with two TMA tile stores, then frees the slot
-//                for the Q warp; other warps store their rows directly.
+//                sends them out with two TMA tile stores; once the TMA unit has
+//                read them (checked at the end of the next unit's first key
+//                tile, off the boundary) the slot is freed for the Q warp.
+//                Other warps store their rows directly.
 // Each 128-key tile is taken in two halves of 64 keys, h = 0, 1, each with
 // its own 64 TMEM columns of S: per query tile the issuer runs PV of half h
 // of key tile j and then QK of half h of key tile j + 1 into the same
@@ -49,7 +51,8 @@
 // the document end in the last tile are masked to -inf, rows past it are
 // never stored.  Each pair runs its own range of the work list (placed on the
 // host longest-processing-time first), and the next unit's first QKs are
-// issued during the current unit's last key tile.
+// issued right after the current unit's last PVs, so its softmax finds them
+// done when it comes back from the epilogue.
 //
 // Key halves: a CTA holds keys [64 rank, 64 rank + 64) of a tile; half h is
 // rows [32 h, 32 h + 32) of both CTAs' halves (the pair MMA takes B's first
@@ -713,16 +716,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // Per key tile j and half h, for each query tile s: wait for P(s, j, h),
         // then PV(s, j, h) and QK(s, j + 1, h) -- the next key tile's S half
         // goes where P(s, j, h) was, and the softmax works on the other half
-        // meanwhile.  In the last key tile the next unit's first QKs take the
-        // place of QK(s, j + 1, h).  The next unit's first key tile is the K
-        // half of this unit's last group (ring slot kslot in the last key
-        // tile); its group is released when the next unit's last query tile
-        // sees S of half 1, so that QK is issued after every PV of this unit
-        // (held back to the end when the next unit has fewer query tiles).
+        // meanwhile.  In the last key tile all PVs go first (the epilogue
+        // waits for them), then the next unit's first QKs.  The next unit's
+        // first key tile is the K half of this unit's last group (ring slot
+        // kslot in the last key tile); its group is released when the next
+        // unit's last query tile sees S of half 1, so that QK comes after
+        // every PV of this unit.
         const bool has_next = u + 1 < u_end;
         const UnitGeom gn = unit_geom(a.units, has_next ? u + 1 : u);
         const uint32_t qn = 2 * ((k + 1) & 1);
-        const bool fewer_next = has_next && gn.n_st < g.n_st;
         const bool two = g.n_st == 2;
         // steady state: key tiles with a next key tile in this unit
         for (int j = g.lo; ok && j + 1 < g.hi; ++j) {
@@ -749,9 +751,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         // the last key tile: each PV is followed by "PV done" of its half (the
-        // epilogue waits for it), and the next unit's first QKs take the place
-        // of QK(s, j + 1, h); the QK that releases the next unit's first K/V
-        // group in the ring comes after every PV of this unit
+        // epilogue waits for both halves); the next unit's first QKs follow
+        // the last PV, so that the epilogue does not wait behind them
         {
           const bool acc0 = g.hi - 1 > g.lo;
           for (int h = 0; ok && h < 2; ++h) {
@@ -764,16 +765,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               dev::tc_fence_after();
               pv_half(s, vslot, h, acc0 || h == 1);
               commit_pair_elect(bars.pv_done(s, h));
-              if (has_next && s < gn.n_st && !(h == 1 && fewer_next && s == gn.n_st - 1)) {
-                first_qk(gn, qn, kslot, s, h);
-                if (!ok) break;
-              }
             }
-            if (!ok) break;
-            if (has_next) {
-              for (int s = 0; ok && s < gn.n_st; ++s)
-                if (s >= g.n_st || (h == 1 && fewer_next && s == gn.n_st - 1)) first_qk(gn, qn, kslot, s, h);
-            }
+          }
+          if (has_next) {
+            for (int h = 0; ok && h < 2; ++h)
+              for (int s = 0; ok && s < gn.n_st; ++s) first_qk(gn, qn, kslot, s, h);
           }
           vslot = vslot + 2 >= (uint32_t)kSlots ? vslot + 2 - kSlots : vslot + 2;
           kslot = kslot + 2 >= (uint32_t)kSlots ? kslot + 2 - kSlots : kslot + 2;
@@ -867,13 +863,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     const float sl2 = a.scale_log2;
     __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.o);
+    // bf16: the Q slot whose staged O rows are still being read by the TMA
+    // unit; it is freed (after the read) at the end of the next unit's first
+    // key tile, off the unit boundary
+    int pending_q = -1;
+    auto release_q = [&]() {
+      if (pending_q >= 0) {
+        __syncwarp();
+        if (lane == 0) {
+          dev::bulk_wait_read_all();
+          dev::mbar_arrive(bars.q_empty(pending_q));
+        }
+        pending_q = -1;
+      }
+    };
     // 32-byte output stores when every row start is 32-byte aligned
     const bool o_wide = (reinterpret_cast<uintptr_t>(a.o) & 31u) == 0 && (a.o_stride & 15) == 0;
     for (int u = u_begin; ok && u < u_end; ++u) {
       const UnitGeom g = unit_geom(a.units, u);
       const uint32_t t_unit = t0;
       t0 += g.hi - g.lo;
-      if (st >= g.n_st) continue;
+      if (st >= g.n_st) {
+        release_q();  // this query tile sits the unit out: free its last Q slot now
+        continue;
+      }
       const uint32_t q_slot = 2 * ((u - u_begin) & 1) + st;  // this unit's Q tile of this query tile
       // ring bookkeeping by one lane of one warp per CTA
       const bool releases = lead_lane && st == g.n_st - 1;
@@ -1086,6 +1099,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               break;
             }
           }
+          release_q();
         }
       }
       if (!ok) break;
@@ -1166,9 +1180,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           dev::tma_store_2d(&tm_o, tile + lane_base * 128u, g.head * kHeadDim, row0);
           dev::tma_store_2d(&tm_o, tile + kQHalfBytes + lane_base * 128u, g.head * kHeadDim + 64, row0);
           dev::bulk_commit();
-          dev::bulk_wait_read_all();  // the slot is read: the next unit's Q may land there
-          dev::mbar_arrive(bars.q_empty(q_slot));
         }
+        pending_q = (int)q_slot;
       } else {
         __nv_bfloat16* dst = og + (int64_t)row * a.o_stride + g.head * kHeadDim;
 #pragma unroll
