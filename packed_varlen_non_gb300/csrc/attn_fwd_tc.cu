@@ -16,10 +16,11 @@
 // K tile and dims [64 rank, 64 rank + 64) of a V tile -- so a CTA reads
 // (and loads from L2) half the key/value bytes a single-CTA kernel would.
 // Per CTA, 11 warps:
-//   warp 9       TMA producer: its halves of the document's K and V tiles
-//                through a 6-slot ring; V(j) and the next K tile form one
-//                group behind one barrier.  (FP8: also its own Q tiles, the
-//                next unit's behind the current unit's first K/V group.)
+//   warp 9       lane 0: TMA producer, its halves of the document's K and V
+//                tiles through a 6-slot ring; V(j) and the next K tile form
+//                one group behind one barrier.  (FP8: also its own Q tiles,
+//                the next unit's behind the current unit's first K/V group.)
+//                lane 1 (bf16): the O-store thread (below).
 //   warp 10      Q warp: loads this CTA's Q tiles (bf16) into double-buffered
 //                slots as they come free, so the next unit's tiles are ready
 //                before it starts; as each lands, applies the fused Q prologue
@@ -34,12 +35,13 @@
 //                writes P as bf16 back into TMEM over its S columns, rescales
 //                its O row when the max has grown by more than 2^8, and at the
 //                end of the unit writes O / l and the log-sum-exp.  A bf16
-//                warp whose 32 rows all lie in the document stages them in
-//                the unit's Q slot (free once the unit's MMAs are done) and
-//                sends them out with two TMA tile stores; once the TMA unit has
-//                read them (checked at the end of the next unit's first key
-//                tile, off the boundary) the slot is freed for the Q warp.
-//                Other warps store their rows directly.
+//                warp whose 32 rows all lie in the document stages them, bf16,
+//                in the unit's Q slot (free once the unit's MMAs are done);
+//                other warps store their rows directly.  Either way the four
+//                warps of a query tile then report to the O-store thread,
+//                which sends the staged rows out with TMA tile stores, waits
+//                until they have read the slot and frees it for the Q warp --
+//                so the softmax warps never wait on the TMA unit.
 // Each 128-key tile is taken in two halves of 64 keys, h = 0, 1, each with
 // its own 64 TMEM columns of S: per query tile the issuer runs PV of half h
 // of key tile j and then QK of half h of key tile j + 1 into the same
@@ -82,8 +84,8 @@
 // waits for the other half's latest PV: through the S-ready of the QK issued
 // right after it, or "PV done" in the last key tile.  Q tiles:
 // the even CTA's "Q ready" barrier counts one arrival from the Q warp of each
-// CTA; a bf16 Q slot's "free" barrier counts the four softmax warps of its
-// query tile in that CTA, after their epilogue.
+// CTA; a bf16 Q slot is freed by the O-store thread after the four softmax
+// warps of its query tile in that CTA have reported their epilogue done.
 //
 // FP8 variant (template argument kFp8, h3attn_forward_fp8): the same kernel
 // on e4m3 Q, K and transposed V (channel rows of keys, every document
@@ -121,8 +123,8 @@ constexpr int kQWarp = 10;
 constexpr int kTileRows = 128;
 constexpr int kSlots = 6;                              // ring slots (16 KB each)
 constexpr int kGroups = kSlots / 2;                    // key/value groups in flight
-// barriers: q_full[4] q_empty[4] q_ready[4] kv_full[G] kv_empty[G] s_ready[2][2] p_ready[2][2] pv_done[2][2] drain
-constexpr int kNumBars = 12 + 2 * kGroups + 4 + 4 + 4 + 1;
+// barriers: q_full[4] q_empty[4] q_ready[4] kv_full[G] kv_empty[G] s_ready[2][2] p_ready[2][2] pv_done[2][2] drain o_staged[4]
+constexpr int kNumBars = 12 + 2 * kGroups + 4 + 4 + 4 + 1 + 4;
 // Shared-memory layout: 2 buffers x 2 query tiles, then the ring.  bf16: a Q
 // tile is 128 rows x 128 dims in two 16 KB halves of 64 dims, a slot 16 KB;
 // fp8 (e4m3): a Q tile is one 16 KB block of 128-byte rows, a slot 8 KB.
@@ -170,6 +172,9 @@ struct Bars {
   // (one phase per unit)
   __device__ uint32_t pv_done(int s, int h) const { return base + 8 * (20 + 2 * kGroups + 2 * s + h); }
   __device__ uint32_t drain() const { return base + 8 * (24 + 2 * kGroups); }
+  // bf16: the four softmax warps of Q slot i's query tile have finished that
+  // unit's epilogue (their O rows staged in the slot or stored)
+  __device__ uint32_t o_staged(int i) const { return base + 8 * (25 + 2 * kGroups + i); }
 };
 
 struct UnitGeom {
@@ -483,10 +488,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     for (int i = 0; i < 4; ++i) {
       dev::mbar_init(bars.q_full(i), 1);
-      // FP8: freed by the MMA issuer after a unit's last QK; bf16: by the four
-      // softmax warps of the tile in each CTA, after their epilogue (which
-      // stages the O tile in the finished unit's Q slot)
-      dev::mbar_init(bars.q_empty(i), kFp8 ? 1 : 4);
+      // FP8: freed by the MMA issuer after a unit's last QK; bf16: by the
+      // O-store thread, once the TMA unit has read the O rows the epilogue
+      // staged in the slot
+      dev::mbar_init(bars.q_empty(i), 1);
+      dev::mbar_init(bars.o_staged(i), 4);
       dev::mbar_init(bars.q_ready(i), 2);           // the Q warp of each CTA of the pair
     }
     for (int s = 0; s < 2; ++s) {
@@ -521,6 +527,44 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp == kTmaWarp) {
     // ------------------------------------------------------ TMA producer ----
+    if (!kFp8 && lane == 1) {
+      // bf16 O stores: as the four softmax warps of a query tile finish a
+      // unit's epilogue, send the rows they staged in its Q slot (every warp
+      // whose 32 rows lie in the document) with TMA tile stores, wait until
+      // they have read the slot, and free it for the Q warp's next load.
+      uint32_t use[4] = {0, 0, 0, 0};
+      bool ok = true;
+      int k = 0;
+      for (int u = u_begin; ok && u < u_end; ++u, ++k) {
+        const UnitGeom g = unit_geom(a.units, u);
+#pragma unroll 1
+        for (int s = 0; s < 2 && s < g.n_st; ++s) {
+          const int i = 2 * (k & 1) + s;
+          ok = dev::mbar_wait(bars.o_staged(i), use[i] & 1, abort_flag, a.err, kTimeoutNs);
+          ++use[i];
+          if (!ok) break;
+          if (o_tma != 0 && g.part < 0) {
+            const uint32_t tile = sbase + C::SmemQ + i * C::QTileBytes;
+            const int32_t base_row = g.q0 + s * 2 * kTileRows + (int32_t)rank * kTileRows;
+            bool any = false;
+#pragma unroll 1
+            for (int w = 0; w < 4; ++w) {
+              const int32_t row0 = base_row + 32 * w;
+              if (row0 + 31 >= g.kv1) break;  // (the softmax warps' own test)
+              dev::tma_store_2d(&tm_o, tile + 32u * w * 128u, g.head * kHeadDim, row0);
+              dev::tma_store_2d(&tm_o, tile + kQHalfBytes + 32u * w * 128u, g.head * kHeadDim + 64, row0);
+              any = true;
+            }
+            if (any) {
+              dev::bulk_commit();
+              dev::bulk_wait_read_all();
+            }
+          }
+          dev::mbar_arrive(bars.q_empty(i));
+        }
+      }
+      dev::bulk_wait_all();  // the O stores are complete
+    }
     if (lane == 0) {
       const uint64_t pol_q = dev::policy_evict_first();
       const uint64_t pol_kv = dev::policy_evict_last();
@@ -863,30 +907,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     bool ok = true;
     const float sl2 = a.scale_log2;
     __nv_bfloat16* og = static_cast<__nv_bfloat16*>(a.o);
-    // bf16: the Q slot whose staged O rows are still being read by the TMA
-    // unit; it is freed (after the read) at the end of the next unit's first
-    // key tile, off the unit boundary
-    int pending_q = -1;
-    auto release_q = [&]() {
-      if (pending_q >= 0) {
-        __syncwarp();
-        if (lane == 0) {
-          dev::bulk_wait_read_all();
-          dev::mbar_arrive(bars.q_empty(pending_q));
-        }
-        pending_q = -1;
-      }
-    };
     // 32-byte output stores when every row start is 32-byte aligned
     const bool o_wide = (reinterpret_cast<uintptr_t>(a.o) & 31u) == 0 && (a.o_stride & 15) == 0;
     for (int u = u_begin; ok && u < u_end; ++u) {
       const UnitGeom g = unit_geom(a.units, u);
       const uint32_t t_unit = t0;
       t0 += g.hi - g.lo;
-      if (st >= g.n_st) {
-        release_q();  // this query tile sits the unit out: free its last Q slot now
-        continue;
-      }
+      if (st >= g.n_st) continue;
       const uint32_t q_slot = 2 * ((u - u_begin) & 1) + st;  // this unit's Q tile of this query tile
       // ring bookkeeping by one lane of one warp per CTA
       const bool releases = lead_lane && st == g.n_st - 1;
@@ -1099,7 +1126,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
               break;
             }
           }
-          release_q();
         }
       }
       if (!ok) break;
@@ -1143,7 +1169,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (valid) a.part_ml[slot] = make_float2(m_used, l);
         if constexpr (!kFp8) {
           __syncwarp();
-          if (lane == 0) dev::mbar_arrive(bars.q_empty(q_slot));
+          if (lane == 0) dev::mbar_arrive(bars.o_staged(q_slot));
         }
         continue;
       }
@@ -1175,13 +1201,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // visible to the TMA unit
         __syncwarp();
-        if (lane == 0) {
-          const int32_t row0 = g.q0 + st * 2 * kTileRows + (int32_t)rank * kTileRows + (int32_t)lane_base;
-          dev::tma_store_2d(&tm_o, tile + lane_base * 128u, g.head * kHeadDim, row0);
-          dev::tma_store_2d(&tm_o, tile + kQHalfBytes + lane_base * 128u, g.head * kHeadDim + 64, row0);
-          dev::bulk_commit();
-        }
-        pending_q = (int)q_slot;
+        if (lane == 0) dev::mbar_arrive(bars.o_staged(q_slot));  // the store thread sends them
       } else {
         __nv_bfloat16* dst = og + (int64_t)row * a.o_stride + g.head * kHeadDim;
 #pragma unroll
@@ -1207,7 +1227,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         if constexpr (!kFp8) {
           __syncwarp();
-          if (lane == 0) dev::mbar_arrive(bars.q_empty(q_slot));
+          if (lane == 0) dev::mbar_arrive(bars.o_staged(q_slot));
         }
       }
       if (valid && a.lse != nullptr)
@@ -1215,8 +1235,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
   }
 
-  if constexpr (!kFp8)
-    if (warp < kMmaWarp && lane == 0) dev::bulk_wait_all();  // the epilogue's TMA stores are complete
   // Neither CTA leaves (or frees the pair's TMEM) while the other may still
   // arrive on its barriers or run MMAs on its shared memory and TMEM.
   dev::tc_fence_before();
