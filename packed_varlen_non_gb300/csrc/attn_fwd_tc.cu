@@ -1152,18 +1152,54 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // reference max (log2 units) and sum, for the merge pass.
         // (the partial buffer is a device allocation: its 512-byte rows are 32-byte aligned)
         const size_t slot = (size_t)g.part * kUnitRows + local;
-        float* dst = a.part_o + slot * kHeadDim;
+        if constexpr (!kFp8) {
+          // bf16: each 32-column chunk of the warp's 32 rows goes through its
+          // rows of the unit's Q slot (free: the slot is released only after
+          // this warp reports), so that every global store writes whole
+          // 128-byte row segments: a store instruction covers 4 rows.
+          const uint32_t stage = sbase + C::SmemQ + q_slot * C::QTileBytes + lane_base * 128u;
+          const size_t slot0 = (size_t)g.part * kUnitRows + (size_t)(local - (int32_t)lane);
+          const int32_t row_first = g.q0 + local - (int32_t)lane;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t ov[32];
+            dev::tmem_ld32(t_o + c * 32, ov);
+            dev::tmem_wait_ld();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t ov[32];
-          dev::tmem_ld32(t_o + c * 32, ov);
-          dev::tmem_wait_ld();
-          if constexpr (kFp8) scale_by_channel(ov, a.sv + g.head * kHeadDim + c * 32);
-          if (valid) {
+            for (int e = 0; e < 8; ++e) {
+              const uint32_t addr = stage + lane * 128u + ((((uint32_t)e) ^ (lane & 7u)) << 4);
+              asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(ov[4 * e]), "r"(ov[4 * e + 1]),
+                           "r"(ov[4 * e + 2]), "r"(ov[4 * e + 3])
+                           : "memory");
+            }
+            __syncwarp();
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              dev::st_global_v8(dst + c * 32 + e * 8, ov[8 * e], ov[8 * e + 1], ov[8 * e + 2], ov[8 * e + 3],
-                                ov[8 * e + 4], ov[8 * e + 5], ov[8 * e + 6], ov[8 * e + 7]);
+            for (int i = 0; i < 8; ++i) {
+              const uint32_t r = 4 * i + (lane >> 3), q = lane & 7u;  // row of the warp, 16-byte piece
+              uint4 v;
+              asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                           : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                           : "r"(stage + r * 128u + ((q ^ (r & 7u)) << 4))
+                           : "memory");
+              if (row_first + (int32_t)r < g.kv1)
+                *reinterpret_cast<uint4*>(a.part_o + (slot0 + r) * kHeadDim + c * 32 + 4 * q) = v;
+            }
+            __syncwarp();
+          }
+        } else {
+          float* dst = a.part_o + slot * kHeadDim;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint32_t ov[32];
+            dev::tmem_ld32(t_o + c * 32, ov);
+            dev::tmem_wait_ld();
+            scale_by_channel(ov, a.sv + g.head * kHeadDim + c * 32);
+            if (valid) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                dev::st_global_v8(dst + c * 32 + e * 8, ov[8 * e], ov[8 * e + 1], ov[8 * e + 2], ov[8 * e + 3],
+                                  ov[8 * e + 4], ov[8 * e + 5], ov[8 * e + 6], ov[8 * e + 7]);
+            }
           }
         }
         if (valid) a.part_ml[slot] = make_float2(m_used, l);
