@@ -297,8 +297,7 @@ h3attn_status h3attn_forward_fp8(h3attn_plan_t plan, const void* q8, const void*
  * except that o must not share any byte range with q, k or v.
  * Calls no cudaMalloc/cudaFree or other allocating routine.  The first call
  * on a device looks up the array's device address (cudaGetSymbolAddress) with
- * that device current; make that first call before any stream capture.  All
- * calls share the array and it keeps the last call's contents: the work list
+ * that device current.  All calls share the array and it keeps the last call's contents: the work list
  * is rewritten and the error word cleared on every call.  Calls from several
  * host threads on one stream are safe: each call enqueues its copy of the
  * work list and its kernel under one lock, so they run in that order.  Calls
