@@ -845,7 +845,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bool good = true;
         if constexpr (!kFp8) {
           // bf16: this warp loads the tile once its slot is free (the
-          // previous unit in the slot has finished its epilogue)
+          // O-store thread has sent the previous unit's O rows out of it)
           if (lane == 0) {
             good = dev::mbar_wait(bars.q_empty(i), (q_use[i] & 1) ^ 1, abort_flag, a.err, kTimeoutNs);
             if (good) {
@@ -1215,7 +1215,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (staged) {
         // The warp's 32 rows, bf16, into its rows of the unit's Q slot (free:
         // every MMA of the unit is done) in the tile's 128-byte swizzled
-        // layout, then two TMA stores (dims 0..63, 64..127) of 32 rows each.
+        // layout; the O-store thread sends them with two TMA stores (dims
+        // 0..63, 64..127) of 32 rows each.
         const uint32_t tile = sbase + C::SmemQ + q_slot * C::QTileBytes;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
